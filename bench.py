@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 NVFP4 4/6 quantizer, as one JSON line.
+
+Headline workload: MoE activations at DeepSeek-V3 width, X bf16 [16384 x 7168], per-token FP32
+scale, Four-Over-Six block scales, fused quantize -> dequantize round trip (codes, E4M3 scales,
+row scales and BF16 y), i.e. one launch of nvfp4_fused_roundtrip per step.  Inputs are drawn on
+the device (seeded) and stay resident; the 235 MB input exceeds the 129 MB L2, so no step reads
+the previous step's data from L2.
+
+  value     algorithmic HBM bytes (2 B in + 0.5625 B codes/scales + 2 B y per element + 4 B per
+            row) per step / device time per step, summed over ranks, in GB/s
+  e2e       the same metric through the public API with pinned host buffers: every step copies
+            x host->device, runs the call, and copies all outputs back
+  roofline  the fused kernel's achieved GB/s against the measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle on a bounded sample of the same rows (single thread)
+  also      kernel-only GB/s of the other workloads (weights, expert-grouped, long rollout)
+
+--impl reference times the CPU oracle instead (the only reference this method has).
+Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no collective on the path).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = 2
+METRIC = "NVFP4 4/6 quantize GB/s and elem/s, fraction of GB300 HBM peak"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def algorithmic_bytes(rows, cols, op, scale_kind="row"):
+    n = rows * cols
+    scale_bytes = 4 * rows if scale_kind == "row" else 4
+    quant = 2 * n + n // 2 + n // 16 + scale_bytes
+    if op == "quantize":
+        return quant
+    if op == "roundtrip":
+        return quant + 2 * n
+    if op == "dequantize":
+        return n // 2 + n // 16 + scale_bytes + 2 * n
+    raise ValueError(op)
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def recorded_traffic(key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    csrc = os.path.join(ROOT, "nvfp4_block_scaled_row_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    digest = h.hexdigest()[:16]
+    try:
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and parts[0] == key and parts[2] == digest:
+                    return float(parts[1])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value, world, device):
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_steps(fn, steps, warmup, world, device):
+    """W warm-up calls, then K timed calls bracketed by barrier + synchronize.  Returns
+    (per-step device ms list, whole-region ms)."""
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    region = starts[0].elapsed_time(ends[-1])
+    return per, region
+
+
+def cpu_baseline(x, op, seconds):
+    """The oracle, as it stands, on a bounded sample of rows of x; single thread."""
+    import numpy as np
+
+    import oracle
+    from nvfp4_block_scaled_row_gb300 import synth
+
+    rows, cols = x.shape
+    probe = synth.as_u16(x[:2])
+    t0 = time.perf_counter()
+    out = oracle.quantize(probe, oracle.MODE_FOUR_OVER_SIX)
+    if op != "quantize":
+        oracle.dequantize(out["codes"], out["scales"], out["scale"])
+    per_row = (time.perf_counter() - t0) / 2
+    n = int(max(4, min(rows, seconds / max(per_row, 1e-6))))
+    idx = np.linspace(0, rows - 1, n).astype(np.int64)
+    sample = synth.as_u16(x[torch.as_tensor(idx, device=x.device)])
+    t0 = time.perf_counter()
+    out = oracle.quantize(sample, oracle.MODE_FOUR_OVER_SIX)
+    if op != "quantize":
+        oracle.dequantize(out["codes"], out["scales"], out["scale"])
+    dt = time.perf_counter() - t0
+    gbs = algorithmic_bytes(n, cols, op) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "elem_per_s": round(n * cols / dt, 1),
+            "sample": f"{n} evenly spaced rows of the {rows}x{cols} workload, "
+                      f"{'quantize+dequantize' if op != 'quantize' else 'quantize'}, "
+                      f"{dt:.1f} s single-threaded"}
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the CPU oracle on the host cores, on the headline workload."""
+    from nvfp4_block_scaled_row_gb300 import synth
+
+    if rank != 0:
+        return
+    w = synth.workload(HEADLINE)
+    x = synth.generate(HEADLINE, device="cuda:0" if torch.cuda.is_available() else "cpu")["x"]
+    import oracle
+
+    rows_per_step = 8
+    total_rows = rows_per_step * (args.steps + args.warmup)
+    idx = torch.linspace(0, x.shape[0] - 1, total_rows).long().to(x.device)
+    xs = synth.as_u16(x[idx])
+    times = []
+    for s in range(args.warmup + args.steps):
+        chunk = xs[s * rows_per_step:(s + 1) * rows_per_step]
+        t0 = time.perf_counter()
+        out = oracle.quantize(chunk, oracle.MODE_FOUR_OVER_SIX)
+        oracle.dequantize(out["codes"], out["scales"], out["scale"])
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    step_bytes = algorithmic_bytes(rows_per_step, w.cols, "roundtrip")
+    sec = statistics.mean(times)
+    value = step_bytes / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name} (workload {w.index}) sample", "rows": x.shape[0],
+                   "cols": w.cols, "rows_per_step": rows_per_step, "op": "roundtrip",
+                   "scale": "row", "mode": "four_over_six"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows_per_step} rows of {x.shape[0]}x{w.cols} per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "elem_per_s": round(rows_per_step * w.cols / sec, 1),
+    }
+    print(json.dumps(line))
+
+
+def bench_op(nv, x, op, kind, mode, steps, warmup, world, device, offsets=None):
+    rows, cols = x.shape
+    if op == "roundtrip":
+        outs = nv.nvfp4_fused_roundtrip(x, kind, mode)
+        codes, scales, scale, y = outs
+        ws = torch.empty(nv.nvfp4_tensor_workspace_bytes(), dtype=torch.uint8, device=device)
+        fn = lambda: nv.nvfp4_fused_roundtrip(x, kind, mode, codes, scales, scale, y, ws)
+    elif op == "quantize" and kind == "row":
+        codes, scales, scale = nv.nvfp4_quantize_rowwise(x, mode, offsets)
+        fn = lambda: nv.nvfp4_quantize_rowwise(x, mode, offsets, codes, scales, scale)
+    elif op == "quantize":
+        codes, scales, scale = nv.nvfp4_quantize_tensor(x, mode)
+        ws = torch.empty(nv.nvfp4_tensor_workspace_bytes(), dtype=torch.uint8, device=device)
+        fn = lambda: nv.nvfp4_quantize_tensor(x, mode, codes, scales, scale, ws)
+    else:  # dequantize
+        codes, scales, scale = (nv.nvfp4_quantize_rowwise(x, mode) if kind == "row"
+                                else nv.nvfp4_quantize_tensor(x, mode))
+        y = torch.empty_like(x)
+        fn = lambda: nv.nvfp4_dequantize(codes, scales, scale, kind, y)
+    per, region = time_steps(fn, steps, warmup, world, device)
+    ms = statistics.mean(per)
+    gbs = algorithmic_bytes(rows, cols, op, kind) / (ms * 1e-3) / 1e9
+    launches = 2 if (kind == "tensor" and op != "dequantize") else 1
+    return {"gbs": gbs, "ms": ms, "region_ms": region, "launches_per_step": launches}
+
+
+def e2e_roundtrip(nv, x, steps, warmup, device):
+    """Public-API round trip with pinned host buffers; copies inside the timed region."""
+    rows, cols = x.shape
+    x_host = x.cpu().pin_memory()
+    x_dev = torch.empty_like(x)
+    codes, scales, scale, y = nv.nvfp4_fused_roundtrip(x)
+    hosts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (codes, scales, scale, y)]
+
+    def step():
+        x_dev.copy_(x_host, non_blocking=True)
+        nv.nvfp4_fused_roundtrip(x_dev, "row", "four_over_six", codes, scales, scale, y)
+        for h, d in zip(hosts, (codes, scales, scale, y)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(device)
+    sec = (time.perf_counter() - t0) / steps
+    h2d = x.numel() * 2
+    d2h = sum(t.numel() * t.element_size() for t in (codes, scales, scale, y))
+    gbs = algorithmic_bytes(rows, cols, "roundtrip") / sec / 1e9
+    return {"value": round(gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(sec * 1e3, 3)}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import nvfp4_block_scaled_row_gb300 as nv
+    from nvfp4_block_scaled_row_gb300 import synth
+
+    nv.library()
+    w = synth.workload(HEADLINE)
+    x = synth.generate(HEADLINE, device=device)["x"]
+    rows, cols = x.shape
+
+    # Headline: fused round trip, timed per launch with events on the launching stream.
+    with ClockSampler(local) as clocks:
+        head = bench_op(nv, x, "roundtrip", "row", "four_over_six", args.steps, args.warmup,
+                        world, device)
+    ms = max_over_ranks(head["ms"], world, device)
+    step_bytes = algorithmic_bytes(rows, cols, "roundtrip")
+    value = world * step_bytes / (ms * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    achieved = step_bytes / (head["ms"] * 1e-3) / 1e9
+    status = nv.nvfp4_get_device_status()
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name} (workload {w.index}): {w.summary}",
+                   "rows": rows, "cols": cols, "op": "fused quantize->dequantize round trip",
+                   "scale": "row (per-token)", "mode": "four_over_six",
+                   "l2": f"inputs larger than L2 ({rows * cols * 2 / 1e6:.0f} MB > 129 MB), no flush",
+                   "parallelism": f"replicas x{world}"},
+        "elem_per_s": round(world * rows * cols / (ms * 1e-3), 1),
+        "frac_of_hbm_peak": round(achieved / peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic("fused_roundtrip_row_moe_activation"),
+                     "kernel": "quantize_kernel<four_over_six, row, fused>",
+                     "bytes_per_launch": step_bytes, "peak_source": f"{peak_src} hbm_gbs"},
+        "gpu_launches": args.steps * head["launches_per_step"],
+        "clocks": clocks.summary(),
+        "device_status": status,
+    }
+
+    if rank == 0:
+        line["e2e"] = e2e_roundtrip(nv, x, max(3, args.steps // 5), 3, device)
+        line["cpu_baseline"] = cpu_baseline(x, "roundtrip", args.cpu_seconds)
+    if not args.no_extras:
+        also = {}
+        del x
+        torch.cuda.empty_cache()
+        for idx, op, kind, mode in ((3, "quantize", "row", "four_over_six"),
+                                    (4, "roundtrip", "row", "four_over_six"),
+                                    (4, "quantize", "row", "four_over_six"),
+                                    (4, "dequantize", "row", "four_over_six"),
+                                    (1, "quantize", "tensor", "four_over_six"),
+                                    (1, "quantize", "tensor", "six"),
+                                    (1, "dequantize", "tensor", "four_over_six"),
+                                    (0, "quantize", "row", "four_over_six")):
+            ww = synth.workload(idx)
+            d = synth.generate(idx, device=device)
+            r = bench_op(nv, d["x"], op, kind, mode, max(5, args.steps // 2), 3, world, device,
+                         d["offsets"] if op == "quantize" and kind == "row" else None)
+            also[f"{ww.name}/{op}/{kind}/{mode}"] = {
+                "gbs": round(r["gbs"], 1), "frac": round(r["gbs"] / peak, 4),
+                "us_per_launch": round(r["ms"] * 1e3, 2),
+                "elem_per_s": round(d["x"].numel() / (r["ms"] * 1e-3), 1),
+                "shape": list(d["x"].shape)}
+            del d
+            torch.cuda.empty_cache()
+        line["also"] = also
+        line["device_status_after_extras"] = nv.nvfp4_get_device_status()
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,157 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 NVFP4 quantization library (libnvfp4_gb300.so).
+ *
+ * What it computes (web pages, cited by title and section):
+ *   "NVFP4 RL" blog post (jianyuh.github.io/nvfp4/2026/07/11/NVFP4-RL):
+ *     Sec. 2 "Baseline: Per-Token Scales & Targeted MoE Quantization" -- every token (row) gets its
+ *       own FP32 scale from its amax over the hidden dimension; FP8 E4M3 block scales; both fused
+ *       into the activation quantization kernel.
+ *     Sec. 3 "Gradient Stability: The Chain-Rule Inconsistency" -- the dequantized backward uses
+ *       DQ(Q(w)), the BF16 value of exactly what the quantizer encoded.
+ *     Sec. 4 "The Four-Over-Six (4/6) Optimization" -- each block maps its max to +-6 or to +-4,
+ *       whichever gives the lower block error; weights use the same scheme.
+ *   "humans& Open-Sources the First Stable 4-Bit RL Training Recipe at 1.73x Speedup",
+ *     "Three instabilities, three fixes" -- per-token activation scaling, dequantized backward,
+ *     4/6 for weights and activations, bit-exact across training and inference.
+ *   "TRACE FP4 RL -- Rollout-guided FP4 rounding", Jargon -- the E2M1 grid
+ *     {0, 0.5, 1, 1.5, 2, 3, 4, 6} and round-to-nearest.
+ *
+ * The exact arithmetic (every FP32 rounding, the 4/6 error order, tie rules) is fixed in the
+ * design notes; results are bit-identical to the CPU oracle that states it.
+ *
+ * Data layout (all row-major, all caller-owned DEVICE memory unless stated otherwise):
+ *   x, y          BF16 [rows][cols], cols a multiple of 16, 16-byte aligned base.
+ *   codes         uint8 [rows][cols/2]: E2M1 codes, element 2j in the low nibble of byte j,
+ *                 16-byte aligned base.
+ *   block_scales  uint8 [rows][cols/16]: one FP8 E4M3 byte per 16-element block.
+ *   row scale     float [rows]: S_dec = amax_row / (6 * M) per row.
+ *   tensor scale  float [1]:    S_dec = amax_tensor / (6 * M).
+ *   M = 256 in mode FOUR_OVER_SIX and 448 in mode SIX.
+ *
+ * Contract common to every call:
+ *   - Asynchronous on `stream` (NULL = the legacy default stream); nothing synchronizes.
+ *   - Arguments are validated on the host before anything is launched; a rejected call launches
+ *     nothing and touches no memory.  rows == 0 is a valid no-op.
+ *   - The library allocates no memory.  Inputs must not overlap outputs.
+ *   - Errors detected on the device (invalid group offsets, a bounded wait that ran out) are
+ *     recorded in a per-device status word read by nvfp4_get_device_status(); the first error
+ *     recorded wins.
+ *   - Non-finite inputs are outside the contract: they do not fault, their outputs are unspecified.
+ *   - Results do not depend on the launch configuration, the stream or the rest of the batch.
+ */
+#ifndef NVFP4_GB300_H
+#define NVFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL selects the legacy default stream. */
+typedef struct CUstream_st* nvfp4_stream_t;
+
+typedef enum {
+  NVFP4_MODE_SIX = 0,           /* block max always mapped to +-6 (ordinary NVFP4)           */
+  NVFP4_MODE_FOUR_OVER_SIX = 1  /* block max mapped to +-6 or +-4, lower block error wins    */
+} nvfp4_mode;
+
+typedef enum {
+  NVFP4_SCALE_ROW = 0,    /* one FP32 scale per row (token)    */
+  NVFP4_SCALE_TENSOR = 1  /* one FP32 scale for the tensor     */
+} nvfp4_scale_kind;
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,  /* null pointer, bad enum, negative count, overlapping buffers   */
+  NVFP4_ERR_SHAPE = 2,        /* cols not a positive multiple of 16, or too large               */
+  NVFP4_ERR_ALIGNMENT = 3,    /* a pointer below its required alignment                         */
+  NVFP4_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed                    */
+  NVFP4_ERR_TIMEOUT = 5,      /* device side: a bounded wait on a shared-memory barrier ran out */
+  NVFP4_ERR_OFFSETS = 6,      /* device side: group offsets not 0 = o[0] <= ... <= o[G] = rows  */
+  NVFP4_ERR_WORKSPACE = 7     /* workspace missing or smaller than nvfp4_tensor_workspace_bytes */
+} nvfp4_status;
+
+/* Per-token quantization ("NVFP4 RL" Sec. 2 and Sec. 4).
+ *   x             BF16 [rows][cols] on the device.
+ *   group_offsets optional device int32 [num_groups + 1] describing expert groups of rows
+ *                 (MoE grouped layout).  Quantization never depends on the grouping; the offsets
+ *                 are validated on the device (0 = o[0] <= o[1] <= ... <= o[num_groups] = rows)
+ *                 and a violation records NVFP4_ERR_OFFSETS.  NULL (with num_groups == 0) skips it.
+ *   mode          NVFP4_MODE_SIX or NVFP4_MODE_FOUR_OVER_SIX.
+ *   codes, block_scales, row_scale   outputs as laid out above.
+ * Supported cols: 16 <= cols <= 32768, cols % 16 == 0. */
+nvfp4_status nvfp4_quantize_rowwise(const void* x, int64_t rows, int64_t cols,
+                                    const int32_t* group_offsets, int32_t num_groups,
+                                    nvfp4_mode mode, uint8_t* codes, uint8_t* block_scales,
+                                    float* row_scale, nvfp4_stream_t stream);
+
+/* Bytes of device workspace the per-tensor calls need (a few KB; it holds partial maxima). */
+size_t nvfp4_tensor_workspace_bytes(void);
+
+/* Per-tensor quantization for weights ("NVFP4 RL" Sec. 4: 4/6 applied to weights as well):
+ * one amax over the whole tensor, then the same block/4-over-6 encoding as the row path.
+ *   tensor_scale  device float [1], receives S_dec.
+ *   workspace     device scratch of at least nvfp4_tensor_workspace_bytes() bytes, 16-byte
+ *                 aligned; its contents on entry are ignored.  Two launches. */
+nvfp4_status nvfp4_quantize_tensor(const void* x, int64_t rows, int64_t cols, nvfp4_mode mode,
+                                   uint8_t* codes, uint8_t* block_scales, float* tensor_scale,
+                                   void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* amax = max |x_i| over n BF16 elements (n >= 0; 0 for n == 0), written to the device float
+ * *amax.  Used by sharded weights: each shard's amax, a max over ranks, then
+ * nvfp4_quantize_tensor_with_amax. */
+nvfp4_status nvfp4_tensor_amax(const void* x, int64_t n, float* amax, void* workspace,
+                               size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* Per-tensor quantization with the amax supplied by the caller (device float [1]), e.g. the
+ * max over shards.  Bit-identical to nvfp4_quantize_tensor when *amax is the tensor's amax. */
+nvfp4_status nvfp4_quantize_tensor_with_amax(const void* x, int64_t rows, int64_t cols,
+                                             nvfp4_mode mode, const float* amax, uint8_t* codes,
+                                             uint8_t* block_scales, float* tensor_scale,
+                                             nvfp4_stream_t stream);
+
+/* Dequantization for the dequantized backward ("NVFP4 RL" Sec. 3):
+ * y = bf16_rne(fp32(fp32(q * s) * S_dec)) for every element -- exactly the value the quantizer
+ * encoded, rounded once to FP32 and once to BF16.
+ *   scale  device float [rows] for NVFP4_SCALE_ROW, [1] for NVFP4_SCALE_TENSOR.
+ *   y      BF16 [rows][cols] output. */
+nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* block_scales,
+                              const float* scale, nvfp4_scale_kind kind, int64_t rows,
+                              int64_t cols, void* y, nvfp4_stream_t stream);
+
+/* Quantize and dequantize in one pass over x: emits codes, block scales, the scale(s) and the
+ * BF16 round trip y = DQ(Q(x)) ("NVFP4 RL" Sec. 2-4).  Outputs are bit-identical to the
+ * separate quantize and dequantize calls.  workspace is needed for NVFP4_SCALE_TENSOR only
+ * (NULL / 0 allowed for NVFP4_SCALE_ROW). */
+nvfp4_status nvfp4_fused_roundtrip(const void* x, int64_t rows, int64_t cols,
+                                   nvfp4_scale_kind kind, nvfp4_mode mode, uint8_t* codes,
+                                   uint8_t* block_scales, float* scale, void* y, void* workspace,
+                                   size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* Reads (and, if clear != 0, resets to NVFP4_OK) the device status word of the current device.
+ * Synchronizes the device.  *status_out receives NVFP4_OK or the first device-side error. */
+nvfp4_status nvfp4_get_device_status(int clear, nvfp4_status* status_out);
+
+/* Static, NUL-terminated description of a status code. */
+const char* nvfp4_status_string(nvfp4_status status);
+
+/* Launch-shape override for tuning and for the launch-independence tests: warps per CTA, ring
+ * stages per warp, and a cap on the grid size; 0 keeps the automatic choice.  Process-wide; the
+ * results never depend on it.  Returns NVFP4_ERR_INVALID_ARG for negative or too-large values. */
+nvfp4_status nvfp4_set_launch_config(int warps_per_cta, int stages, int max_ctas);
+
+/* Self-test of the device-side failure path: launches one warp that waits on a shared-memory
+ * barrier nothing arrives on, giving up after `timeout_ns` nanoseconds (1 ms default if 0) and
+ * recording NVFP4_ERR_TIMEOUT in the device status word.  The wait always ends. */
+nvfp4_status nvfp4_selftest_wait_timeout(uint64_t timeout_ns, nvfp4_stream_t stream);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int nvfp4_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GB300_H */

@@ -1,0 +1,280 @@
+// nvfp4_device.cuh -- device-side building blocks for the sm_103a NVFP4 kernels: shared-memory
+// barriers and bulk (TMA) copies, the hardware FP32 <-> E2M1 / E4M3 / BF16 conversions, packed
+// FP32x2 arithmetic, and the launch-parameter structs shared by the kernel translation units.
+//
+// Every floating-point operation on the quantizer's data path is written as one explicit
+// round-to-nearest instruction (inline PTX or __f*_rn intrinsics), and the library is compiled
+// with --fmad=false, so no multiply-add is ever contracted behind the spec's back.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+constexpr int kBlockElems = 16;          // elements per E4M3-scaled block
+constexpr int kMaxCols = 32768;          // widest row the shared-memory ring supports
+constexpr int kMaxWarpsPerCta = 8;
+constexpr int kMaxStages = 8;
+constexpr int kTableBytes = 256 * 16;    // one ScaleEntry per E4M3 byte
+constexpr int kBarrierBytes = kMaxWarpsPerCta * kMaxStages * 8;
+constexpr int kAmaxMaxPartials = 1024;   // per-tensor amax: partial maxima in the workspace
+
+// Device status codes (same numbers as nvfp4_status in include/nvfp4.h).
+constexpr int kStatusTimeout = 5;
+constexpr int kStatusOffsets = 6;
+
+// Mode numbers (same as nvfp4_mode).
+constexpr int kModeSix = 0;
+constexpr int kModeFourOverSix = 1;
+
+// Per E4M3 byte: the scale s, its correctly rounded reciprocal (0 for s == 0), and -s and +s as
+// FP16 pairs (E4M3 values are exact in FP16).
+struct __align__(16) ScaleEntry {
+  float s;
+  float inv;
+  uint32_t neg_s_h2;
+  uint32_t s_h2;
+};
+
+struct QuantParams {
+  const uint16_t* x;        // BF16 bits [rows][cols]
+  int64_t rows;
+  int32_t cols;
+  uint8_t* codes;           // [rows][cols/2]
+  uint8_t* scales;          // [rows][cols/16]
+  float* scale_out;         // S_dec: [rows] (row scale) or [1] (tensor scale)
+  uint16_t* y;              // BF16 bits [rows][cols], fused round trip only
+  const float* amax_src;    // tensor scale: n_amax partial maxima (or one amax)
+  int32_t n_amax;
+  const int32_t* offsets;   // optional group offsets [num_groups + 1]
+  int32_t num_groups;
+  int32_t stages;           // ring slots per warp
+  uint32_t slot_bytes;      // bytes per ring slot (>= 2*cols, multiple of 128)
+  int* status;              // device status word
+  uint64_t timeout_ns;      // bound on every barrier wait
+};
+
+struct DequantParams {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* scale;       // [rows] or [1]
+  int64_t rows;
+  int32_t cols;
+  uint16_t* y;
+};
+
+// ------------------------------------------------------------------------------------------------
+// Status word
+// ------------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);  // first error wins
+}
+
+// ------------------------------------------------------------------------------------------------
+// Shared-memory barriers and bulk copies (cp.async.bulk, the non-tensor TMA path)
+// ------------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Makes barrier initialisation visible to the async proxy (the bulk-copy engine).
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for the barrier phase with the given parity; gives up after timeout_ns nanoseconds.
+// Returns false when it gave up.  Every wait in this library goes through here.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t start = global_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - start > timeout_ns) return false;
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
+
+// Bulk copy global -> shared, completing on `bar` (bytes: multiple of 16, both ends 16-aligned).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// ------------------------------------------------------------------------------------------------
+// Packed FP32 pairs (.x in the low 32 bits)
+// ------------------------------------------------------------------------------------------------
+
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack2(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Two BF16 values (element 2j in the low half) widened exactly to an FP32 pair.
+__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) {
+  return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// ------------------------------------------------------------------------------------------------
+// Format conversions (hardware, round-to-nearest-even, saturating where named)
+// ------------------------------------------------------------------------------------------------
+
+// max(|a|, |b|) per BF16 half, sign bits = XOR of the inputs' (callers mask them off).
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Largest |value| of a BF16 pair word as FP32 (exact).
+__device__ __forceinline__ float abs_max_of_pair(uint32_t m2) {
+  const uint32_t h = m2 & 0x7FFF7FFFu;
+  const uint32_t top = max(h >> 16, h & 0xFFFFu);
+  return __uint_as_float(top << 16);
+}
+
+// E4M3 (RNE, satfinite) of two FP32 values: `hi` lands in bits 15..8, `lo` in bits 7..0.
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float hi, float lo) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Two E4M3 bytes (bits 15..8 and 7..0) to an FP16 pair (high half, low half); exact.
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two_bytes) {
+  uint32_t d;
+  const uint16_t b = static_cast<uint16_t>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(b));
+  return d;
+}
+
+// Eight FP32 targets (as four pairs, element 2j in .x) to eight E2M1 codes packed in a word,
+// element i in nibble i (RNE, satfinite, sign kept).
+__device__ __forceinline__ uint32_t e2m1x8_from_f32x2(f32x2 p0, f32x2 p1, f32x2 p2, f32x2 p3) {
+  float a0, a1, b0, b1, c0, c1, d0, d1;
+  unpack2(p0, a0, a1);
+  unpack2(p1, b0, b1);
+  unpack2(p2, c0, c1);
+  unpack2(p3, d0, d1);
+  uint32_t w;
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+      : "=r"(w)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1), "f"(d0), "f"(d1));
+  return w;
+}
+
+// Eight E2M1 codes (nibble i = element i) to four FP16 pairs (element 2j in the low half).
+__device__ __forceinline__ void f16x2_from_e2m1x8(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "mov.b32 {q0, q1, q2, q3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, q0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, q1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, q2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, q3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// Per half: a.h * b.h + c (FP16 operands widened exactly, one FP32 rounding) -> FP32 pair.
+__device__ __forceinline__ f32x2 fma_f16x2_f32x2(uint32_t a, uint32_t b, f32x2 c) {
+  float c0, c1, d0, d1;
+  unpack2(c, c0, c1);
+  asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %2;\n\t"
+      "mov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %4;\n\t"
+      "fma.rn.f32.f16 %1, ah, bh, %5;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "r"(a), "r"(b), "f"(c0), "f"(c1));
+  return pack2(d0, d1);
+}
+
+// FP32 pair to BF16 pair (RNE): .x to the low half.
+__device__ __forceinline__ uint32_t bf16x2_from_f32x2(f32x2 v) {
+  float lo, hi;
+  unpack2(v, lo, hi);
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// E4M3 byte -> table entry (built once per CTA).
+__device__ __forceinline__ ScaleEntry make_scale_entry(uint32_t byte) {
+  const uint32_t h2 = f16x2_from_e4m3x2(byte | (byte << 8));  // (s, s) in FP16
+  const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+  ScaleEntry e;
+  e.s = s;
+  e.inv = (s == 0.0f || !(s == s)) ? 0.0f : __frcp_rn(s);
+  e.s_h2 = h2;
+  e.neg_s_h2 = h2 ^ 0x80008000u;
+  return e;
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,42 @@
+// nvfp4_internal.h -- host-side interface between the C ABI (nvfp4_capi.cu) and the kernel
+// translation units.  Not installed; the public interface is include/nvfp4.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "nvfp4_device.cuh"
+
+namespace nvfp4 {
+
+// Launch-shape overrides (0 = automatic), set through nvfp4_set_launch_config.
+struct LaunchOverride {
+  int warps_per_cta;
+  int stages;
+  int max_ctas;
+};
+LaunchOverride launch_override();
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count(int device);
+
+// Quantize: row scale (kTensor = false) or tensor scale, plain or fused round trip.
+// Chooses the ring shape from cols; returns cudaErrorInvalidValue when cols cannot be staged.
+cudaError_t launch_quantize(int mode, bool tensor_scale, bool fused, QuantParams p,
+                            cudaStream_t stream);
+
+// Whether the quantize kernels can stage a row of `cols` BF16 values.
+bool quantize_cols_supported(int64_t cols);
+
+cudaError_t launch_dequantize(bool tensor_scale, const DequantParams& p, cudaStream_t stream);
+
+// Partial maxima of |x| over n BF16 values into `partials`; returns how many were written.
+cudaError_t launch_amax_partials(const uint16_t* x, int64_t n, float* partials, int* n_partials,
+                                 cudaStream_t stream);
+
+// Reduces n partial maxima into *out.
+cudaError_t launch_amax_finalize(const float* partials, int n, float* out, cudaStream_t stream);
+
+cudaError_t launch_wait_timeout_selftest(int* status, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace nvfp4

@@ -1,0 +1,339 @@
+// nvfp4_quant.cu -- the NVFP4 quantize kernels for sm_103a: per-token ("NVFP4 RL" blog, Sec. 2)
+// or per-tensor FP32 scale, E4M3 block scales with Four-Over-Six selection (Sec. 4), packed E2M1
+// codes, and optionally the BF16 dequantized round trip (Sec. 3) in the same pass.
+//
+// Shape of the computation.  The path is bound by HBM bandwidth: every element is read once (2 B)
+// and written once (0.5625 B, plus 2 B for the round trip).  A persistent grid of warps walks the
+// rows; each warp owns a ring of shared-memory slots, one BF16 row per slot, filled by bulk
+// asynchronous copies (cp.async.bulk, the non-tensor TMA path) that complete on per-slot
+// mbarriers.  While the warp encodes row k, rows k+1 .. k+stages-1 are in flight.  Per row:
+//   pass 1  row amax from shared memory (packed BF16x2 |max|, then a warp shuffle reduction);
+//   pass 2  one lane per 16-element block: block amax, both candidate E4M3 scales, E2M1 codes
+//           for both candidates, their block squared errors, the 4/6 choice, and the stores.
+// Lanes of a quarter-warp read alternate 16-byte halves of their 32-byte blocks first, which
+// keeps every 128-bit shared-memory read free of bank conflicts.  The errors are summed in the
+// fixed order the spec prescribes (four FMA chains, then a pairwise combine), so the result is
+// bit-identical to the CPU oracle and independent of the launch shape.
+#include <cfloat>
+
+#include "nvfp4_device.cuh"
+#include "nvfp4_internal.h"
+
+namespace nvfp4 {
+namespace {
+
+struct RowFactors {
+  float S_enc;  // 6M / a: maps the amax to E2M1_MAXVAL * M
+  float c6;     // M / a:   block amax -> scale-to-6 E4M3 scale
+  float c4;     // 1.5M / a: block amax -> scale-to-4 E4M3 scale
+  float S_dec;  // a / 6M:  the stored FP32 dequant multiplier
+};
+
+// "NVFP4 RL" Sec. 4, candidate = fp4 * fp8_scale * amax / (E2M1_MAXVAL * E4M3_4OVER6_MAXVAL),
+// with E4M3_4OVER6_MAXVAL = M = 256 (448 in plain mode six).  Each factor is one IEEE division,
+// clamped to FLT_MAX when it overflows; a zero amax gives all-zero factors.
+template <int kMode>
+__device__ __forceinline__ RowFactors row_factors(float a) {
+  constexpr float M = (kMode == kModeFourOverSix) ? 256.0f : 448.0f;
+  RowFactors f;
+  if (a == 0.0f) {
+    f.S_enc = f.c6 = f.c4 = f.S_dec = 0.0f;
+    return f;
+  }
+  f.S_enc = fminf(__fdiv_rn(6.0f * M, a), FLT_MAX);
+  f.c6 = fminf(__fdiv_rn(M, a), FLT_MAX);
+  f.c4 = fminf(__fdiv_rn(1.5f * M, a), FLT_MAX);
+  f.S_dec = __fdiv_rn(a, 6.0f * M);
+  return f;
+}
+
+// One candidate (scale-to-6 or scale-to-4) for a block whose targets z are held as 8 FP32
+// pairs (pairs 0-3: half A, pairs 4-7: half B).  Produces the two packed code words, the 8
+// decoded FP16 pairs, and the block squared error
+//   e = (E[A][even] + E[A][odd]) + (E[B][even] + E[B][odd]),
+// each E an FMA chain over every second element of the half, in ascending order.
+struct Candidate {
+  uint32_t cw[2];
+  uint32_t r[8];
+  float err;
+};
+
+__device__ __forceinline__ Candidate encode_candidate(const f32x2 (&z)[8], const ScaleEntry e) {
+  Candidate c;
+  const f32x2 inv2 = pack2(e.inv, e.inv);
+  f32x2 t[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) t[j] = mul2(z[j], inv2);  // target scaled down by 1/s
+  c.cw[0] = e2m1x8_from_f32x2(t[0], t[1], t[2], t[3]);
+  c.cw[1] = e2m1x8_from_f32x2(t[4], t[5], t[6], t[7]);
+  uint32_t rA[4], rB[4];
+  f16x2_from_e2m1x8(c.cw[0], rA);
+  f16x2_from_e2m1x8(c.cw[1], rB);
+  f32x2 accA = pack2(0.0f, 0.0f), accB = pack2(0.0f, 0.0f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const f32x2 dA = fma_f16x2_f32x2(rA[j], e.neg_s_h2, z[j]);      // z - r*s, one rounding
+    const f32x2 dB = fma_f16x2_f32x2(rB[j], e.neg_s_h2, z[4 + j]);
+    accA = fma2(dA, dA, accA);
+    accB = fma2(dB, dB, accB);
+    c.r[j] = rA[j];
+    c.r[4 + j] = rB[j];
+  }
+  float a0, a1, b0, b1;
+  unpack2(accA, a0, a1);
+  unpack2(accB, b0, b1);
+  c.err = __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(b0, b1));
+  return c;
+}
+
+template <int kMode, bool kTensor, bool kFused>
+__global__ void __launch_bounds__(256, 1) quantize_kernel(const QuantParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  ScaleEntry* tab = reinterpret_cast<ScaleEntry*>(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTableBytes);
+  unsigned char* ring = smem + kTableBytes + kBarrierBytes;
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int S = p.stages;
+  uint64_t* my_bars = bars + warp * S;
+  unsigned char* my_ring = ring + static_cast<size_t>(warp) * S * p.slot_bytes;
+
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) tab[i] = make_scale_entry(i);
+  if (lane == 0)
+    for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
+  fence_barrier_init();
+  __syncthreads();
+
+  // Group offsets only need validating: every row is quantized independently of its group.
+  if (p.offsets != nullptr && blockIdx.x == 0 && warp == 0) {
+    bool bad = false;
+    for (int i = lane; i <= p.num_groups; i += 32) {
+      const int32_t v = p.offsets[i];
+      if (i == 0 && v != 0) bad = true;
+      if (i == p.num_groups && static_cast<int64_t>(v) != p.rows) bad = true;
+      if (i > 0 && p.offsets[i - 1] > v) bad = true;
+    }
+    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) record_status(p.status, kStatusOffsets);
+  }
+
+  const int cols = p.cols;
+  const int nblk = cols / kBlockElems;
+  const uint32_t row_bytes = static_cast<uint32_t>(cols) * 2u;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
+  const int64_t NW = static_cast<int64_t>(gridDim.x) * nwarps;
+  const uint64_t policy = l2_evict_first_policy();
+  const int h0 = (lane >> 2) & 1;  // which 16-byte half of its block this lane reads first
+
+  RowFactors f{};
+  if (kTensor) {
+    float a = 0.0f;
+    for (int i = lane; i < p.n_amax; i += 32) a = fmaxf(a, p.amax_src[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+    f = row_factors<kMode>(a);
+    if (blockIdx.x == 0 && threadIdx.x == 0) p.scale_out[0] = f.S_dec;
+  }
+
+  // Prologue: fill the ring.
+  int64_t issued = 0;
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) {
+      const int64_t row = gw + s * NW;
+      if (row >= p.rows) break;
+      mbar_arrive_expect_tx(&my_bars[s], row_bytes);
+      bulk_load(my_ring + static_cast<size_t>(s) * p.slot_bytes, p.x + row * cols, row_bytes,
+                &my_bars[s], policy);
+      ++issued;
+    }
+  }
+
+  int64_t k = 0;
+  for (int64_t row = gw; row < p.rows; row += NW, ++k) {
+    const int slot = static_cast<int>(k % S);
+    const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait_bounded(&my_bars[slot], parity, p.timeout_ns) ? 1 : 0;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) {
+      // A copy did not land in time: record it, give the copies still in flight one more
+      // bounded wait so none lands after this warp is gone, and stop.
+      if (lane == 0) {
+        record_status(p.status, kStatusTimeout);
+        for (int64_t i = k; i < issued; ++i)
+          (void)mbar_wait_bounded(&my_bars[i % S], static_cast<uint32_t>((i / S) & 1),
+                                  p.timeout_ns);
+      }
+      return;
+    }
+    const unsigned char* xs = my_ring + static_cast<size_t>(slot) * p.slot_bytes;
+
+    if (!kTensor) {
+      // Pass 1: row amax.
+      uint32_t m2 = 0;
+      for (int b = lane; b < nblk; b += 32) {
+        const uint4 A = *reinterpret_cast<const uint4*>(xs + b * 32 + h0 * 16);
+        const uint4 B = *reinterpret_cast<const uint4*>(xs + b * 32 + (1 - h0) * 16);
+        m2 = max_abs_bf16x2(m2, max_abs_bf16x2(max_abs_bf16x2(A.x, A.y), max_abs_bf16x2(A.z, A.w)));
+        m2 = max_abs_bf16x2(m2, max_abs_bf16x2(max_abs_bf16x2(B.x, B.y), max_abs_bf16x2(B.z, B.w)));
+      }
+      float a = abs_max_of_pair(m2);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+      f = row_factors<kMode>(a);
+      if (lane == 0) p.scale_out[row] = f.S_dec;
+    }
+
+    // Pass 2: encode.
+    const f32x2 senc2 = pack2(f.S_enc, f.S_enc);
+    uint8_t* codes_row = p.codes + row * (cols / 2);
+    uint8_t* scales_row = p.scales + row * nblk;
+    for (int b = lane; b < nblk; b += 32) {
+      const uint4 A = *reinterpret_cast<const uint4*>(xs + b * 32 + h0 * 16);
+      const uint4 B = *reinterpret_cast<const uint4*>(xs + b * 32 + (1 - h0) * 16);
+      const uint32_t mx = max_abs_bf16x2(
+          max_abs_bf16x2(max_abs_bf16x2(A.x, A.y), max_abs_bf16x2(A.z, A.w)),
+          max_abs_bf16x2(max_abs_bf16x2(B.x, B.y), max_abs_bf16x2(B.z, B.w)));
+      const float m = abs_max_of_pair(mx);
+      const float u6 = __fmul_rn(m, f.c6);
+      const float u4 = (kMode == kModeFourOverSix) ? __fmul_rn(m, f.c4) : 0.0f;
+      const uint32_t sb = e4m3x2_from_f32(u4, u6);
+      const uint32_t b6 = sb & 0xFFu, b4 = sb >> 8;
+
+      f32x2 z[8];
+      z[0] = mul2(bf16x2_to_f32x2(A.x), senc2);
+      z[1] = mul2(bf16x2_to_f32x2(A.y), senc2);
+      z[2] = mul2(bf16x2_to_f32x2(A.z), senc2);
+      z[3] = mul2(bf16x2_to_f32x2(A.w), senc2);
+      z[4] = mul2(bf16x2_to_f32x2(B.x), senc2);
+      z[5] = mul2(bf16x2_to_f32x2(B.y), senc2);
+      z[6] = mul2(bf16x2_to_f32x2(B.z), senc2);
+      z[7] = mul2(bf16x2_to_f32x2(B.w), senc2);
+
+      const ScaleEntry e6 = tab[b6];
+      const Candidate c6 = encode_candidate(z, e6);
+      bool pick4 = false;
+      Candidate c4{};
+      ScaleEntry e4{};
+      if (kMode == kModeFourOverSix) {
+        e4 = tab[b4];
+        c4 = encode_candidate(z, e4);
+        pick4 = c4.err < c6.err;  // ties go to 6
+      }
+      const uint32_t wA = pick4 ? c4.cw[0] : c6.cw[0];
+      const uint32_t wB = pick4 ? c4.cw[1] : c6.cw[1];
+      *reinterpret_cast<uint2*>(codes_row + b * 8) = h0 ? make_uint2(wB, wA) : make_uint2(wA, wB);
+      scales_row[b] = static_cast<uint8_t>(pick4 ? b4 : b6);
+
+      if (kFused) {
+        const uint32_t s_h2 = pick4 ? e4.s_h2 : e6.s_h2;
+        const f32x2 sdec2 = pack2(f.S_dec, f.S_dec);
+        const f32x2 nzero = pack2(-0.0f, -0.0f);
+        uint32_t out[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t r = pick4 ? c4.r[j] : c6.r[j];
+          const f32x2 qs = fma_f16x2_f32x2(r, s_h2, nzero);  // q*s, exact
+          out[j] = bf16x2_from_f32x2(mul2(qs, sdec2));
+        }
+        uint16_t* y_blk = p.y + row * cols + b * kBlockElems;
+        *reinterpret_cast<uint4*>(y_blk + h0 * 8) = make_uint4(out[0], out[1], out[2], out[3]);
+        *reinterpret_cast<uint4*>(y_blk + (1 - h0) * 8) = make_uint4(out[4], out[5], out[6], out[7]);
+      }
+    }
+
+    // Slot consumed: refill it with the row `stages` steps ahead.
+    __syncwarp();
+    if (lane == 0) {
+      const int64_t next = row + static_cast<int64_t>(S) * NW;
+      if (next < p.rows) {
+        mbar_arrive_expect_tx(&my_bars[slot], row_bytes);
+        bulk_load(my_ring + static_cast<size_t>(slot) * p.slot_bytes, p.x + next * cols, row_bytes,
+                  &my_bars[slot], policy);
+        ++issued;
+      }
+    }
+  }
+}
+
+struct RingShape {
+  int warps;
+  int stages;
+  uint32_t slot_bytes;
+  size_t smem;
+};
+
+constexpr size_t kSmemLimit = 227 * 1024;
+constexpr int kDefaultWarps = 8;
+
+bool choose_ring(int64_t cols, RingShape* out) {
+  const uint32_t slot = static_cast<uint32_t>(((cols * 2 + 127) / 128) * 128);
+  const size_t avail = kSmemLimit - kTableBytes - kBarrierBytes;
+  const LaunchOverride ov = launch_override();
+  int stages = ov.stages > 0 ? ov.stages : (slot <= 4096 ? 4 : (slot <= 8192 ? 3 : 2));
+  int warps = 0;
+  for (; stages >= 1; --stages) {
+    warps = static_cast<int>(avail / (static_cast<size_t>(stages) * slot));
+    if (warps >= 1) break;
+  }
+  if (stages < 1 || warps < 1) return false;
+  warps = warps < kDefaultWarps ? warps : kDefaultWarps;
+  if (ov.warps_per_cta > 0 && ov.warps_per_cta < warps) warps = ov.warps_per_cta;
+  out->warps = warps;
+  out->stages = stages;
+  out->slot_bytes = slot;
+  out->smem = kTableBytes + kBarrierBytes + static_cast<size_t>(warps) * stages * slot;
+  return true;
+}
+
+template <int kMode, bool kTensor, bool kFused>
+cudaError_t launch_impl(QuantParams p, cudaStream_t stream) {
+  RingShape rs;
+  if (!choose_ring(p.cols, &rs)) return cudaErrorInvalidValue;
+  auto kern = quantize_kernel<kMode, kTensor, kFused>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemLimit));
+  if (err != cudaSuccess) return err;
+  int device = 0;
+  if ((err = cudaGetDevice(&device)) != cudaSuccess) return err;
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, rs.warps * 32, rs.smem);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  int64_t grid = (p.rows + rs.warps - 1) / rs.warps;
+  const int64_t cap = static_cast<int64_t>(sm_count(device)) * per_sm;
+  if (grid > cap) grid = cap;
+  const LaunchOverride ov = launch_override();
+  if (ov.max_ctas > 0 && grid > ov.max_ctas) grid = ov.max_ctas;
+  if (grid < 1) grid = 1;
+  p.stages = rs.stages;
+  p.slot_bytes = rs.slot_bytes;
+  kern<<<static_cast<unsigned>(grid), rs.warps * 32, rs.smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool quantize_cols_supported(int64_t cols) {
+  RingShape rs;
+  return cols > 0 && cols <= kMaxCols && cols % kBlockElems == 0 && choose_ring(cols, &rs);
+}
+
+cudaError_t launch_quantize(int mode, bool tensor_scale, bool fused, QuantParams p,
+                            cudaStream_t stream) {
+  if (mode == kModeFourOverSix) {
+    if (tensor_scale)
+      return fused ? launch_impl<kModeFourOverSix, true, true>(p, stream)
+                   : launch_impl<kModeFourOverSix, true, false>(p, stream);
+    return fused ? launch_impl<kModeFourOverSix, false, true>(p, stream)
+                 : launch_impl<kModeFourOverSix, false, false>(p, stream);
+  }
+  if (tensor_scale)
+    return fused ? launch_impl<kModeSix, true, true>(p, stream)
+                 : launch_impl<kModeSix, true, false>(p, stream);
+  return fused ? launch_impl<kModeSix, false, true>(p, stream)
+               : launch_impl<kModeSix, false, false>(p, stream);
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,289 @@
+"""GPU parity: the CUDA library against the CPU oracle, bit for bit, through the C ABI.
+
+Codes, E4M3 block scales, FP32 scales and dequantized BF16 are integer/byte results of a fully
+specified FP32 computation, so the bar is exact equality everywhere.  Full-size workloads are run
+in the benchmark's launch configuration and checked on sampled rows (the oracle is slow), plus
+properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import nvfp4_block_scaled_row_gb300 as nv
+from nvfp4_block_scaled_row_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+F4, SIX = "four_over_six", "six"
+OMODE = {F4: oracle.MODE_FOUR_OVER_SIX, SIX: oracle.MODE_SIX}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    nv.library()
+    nv.nvfp4_set_launch_config(0, 0, 0)
+    nv.nvfp4_get_device_status(clear=True)
+    yield
+    nv.nvfp4_set_launch_config(0, 0, 0)
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _y_u16(y):
+    return synth.as_u16(y)
+
+
+def _assert_equal(got, want, what):
+    got, want = np.asarray(got), np.asarray(want)
+    if got.dtype == np.float32:
+        got, want = got.view(np.uint32), want.view(np.uint32)
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        i = tuple(bad[0])
+        raise AssertionError(f"{what}: {len(bad)} mismatches, first at {i}: "
+                             f"gpu={got[i]!r} oracle={want[i]!r}")
+
+
+def check_rowwise(x, mode=F4, fused=True, dequant=True):
+    xb = synth.as_u16(x)
+    want = oracle.quantize(xb, OMODE[mode], oracle.SCALE_ROW)
+    codes, scales, sdec = nv.nvfp4_quantize_rowwise(x, mode)
+    torch.cuda.synchronize()
+    _assert_equal(_np(codes), want["codes"], "codes")
+    _assert_equal(_np(scales), want["scales"], "block scales")
+    _assert_equal(_np(sdec), want["scale"], "row scale")
+    ywant = oracle.dequantize(want["codes"], want["scales"], want["scale"], oracle.SCALE_ROW)
+    if dequant:
+        y = nv.nvfp4_dequantize(codes, scales, sdec, "row")
+        _assert_equal(_y_u16(y), ywant, "dequantized y")
+    if fused:
+        c2, s2, d2, y2 = nv.nvfp4_fused_roundtrip(x, "row", mode)
+        _assert_equal(_np(c2), want["codes"], "fused codes")
+        _assert_equal(_np(s2), want["scales"], "fused block scales")
+        _assert_equal(_np(d2), want["scale"], "fused row scale")
+        _assert_equal(_y_u16(y2), ywant, "fused y")
+    assert nv.nvfp4_get_device_status() == 0
+
+
+def check_tensor(x, mode=F4):
+    xb = synth.as_u16(x)
+    want = oracle.quantize(xb, OMODE[mode], oracle.SCALE_TENSOR)
+    ywant = oracle.dequantize(want["codes"], want["scales"], want["scale"], oracle.SCALE_TENSOR)
+    codes, scales, ts = nv.nvfp4_quantize_tensor(x, mode)
+    _assert_equal(_np(codes), want["codes"], "codes")
+    _assert_equal(_np(scales), want["scales"], "block scales")
+    _assert_equal(_np(ts), want["scale"], "tensor scale")
+    y = nv.nvfp4_dequantize(codes, scales, ts, "tensor")
+    _assert_equal(_y_u16(y), ywant, "dequantized y")
+    c2, s2, t2, y2 = nv.nvfp4_fused_roundtrip(x, "tensor", mode)
+    _assert_equal(_np(c2), want["codes"], "fused codes")
+    _assert_equal(_np(s2), want["scales"], "fused block scales")
+    _assert_equal(_np(t2), want["scale"], "fused tensor scale")
+    _assert_equal(_y_u16(y2), ywant, "fused y")
+    amax = nv.nvfp4_tensor_amax(x)
+    assert float(amax.item()) == oracle.amax(xb)
+    c3, s3, t3 = nv.nvfp4_quantize_tensor_with_amax(x, amax, mode)
+    _assert_equal(_np(c3), want["codes"], "with-amax codes")
+    _assert_equal(_np(s3), want["scales"], "with-amax block scales")
+    _assert_equal(_np(t3), want["scale"], "with-amax tensor scale")
+    assert nv.nvfp4_get_device_status() == 0
+
+
+# ---- the five workloads ------------------------------------------------------------------------
+
+def test_workload0_activation_tiny_full():
+    check_rowwise(synth.generate(0, device=DEV)["x"])
+
+
+@pytest.mark.parametrize("mode", [SIX, F4])
+def test_workload1_weight_tensor_scale_full(mode):
+    check_tensor(synth.generate(1, device=DEV)["x"], mode)
+
+
+@pytest.mark.parametrize("index,rows", [(2, 300), (3, 640), (4, 500)])
+def test_workloads_small_instances(index, rows):
+    d = synth.generate(index, device=DEV, rows=rows)
+    check_rowwise(d["x"])
+    check_rowwise(d["x"], SIX, fused=False, dequant=False)
+
+
+def _sample_rows(rows, n=48, seed=0):
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(rows, size=min(n, rows), replace=False).tolist())
+    pick |= {0, rows - 1}
+    return np.array(sorted(pick))
+
+
+def _check_sampled(x, codes, scales, sdec, y, rows_idx):
+    xs = synth.as_u16(x[torch.as_tensor(rows_idx, device=x.device)])
+    want = oracle.quantize(xs, oracle.MODE_FOUR_OVER_SIX, oracle.SCALE_ROW)
+    idx = torch.as_tensor(rows_idx, device=x.device)
+    _assert_equal(_np(codes[idx]), want["codes"], "sampled codes")
+    _assert_equal(_np(scales[idx]), want["scales"], "sampled block scales")
+    _assert_equal(_np(sdec[idx]), want["scale"], "sampled row scale")
+    if y is not None:
+        ywant = oracle.dequantize(want["codes"], want["scales"], want["scale"])
+        _assert_equal(_y_u16(y[idx]), ywant, "sampled y")
+
+
+@pytest.mark.parametrize("index", [2, 3, 4])
+def test_full_size_sampled_rows(index):
+    """Full-size workloads in the benchmark's launch configuration, checked on sampled rows,
+    plus: the separate dequantize equals the fused round trip on every element."""
+    d = synth.generate(index, device=DEV)
+    x = d["x"]
+    rows = x.shape[0]
+    codes, scales, sdec, y = nv.nvfp4_fused_roundtrip(x, "row", F4)
+    c1, s1, d1 = nv.nvfp4_quantize_rowwise(x, F4, group_offsets=d["offsets"])
+    assert torch.equal(c1, codes) and torch.equal(s1, scales) and torch.equal(d1, sdec)
+    y2 = nv.nvfp4_dequantize(codes, scales, sdec, "row")
+    assert torch.equal(y2.view(torch.int16), y.view(torch.int16))
+    picks = _sample_rows(rows, seed=index)
+    if index == 4:
+        zero_rows = torch.nonzero(x.abs().amax(1) == 0).flatten()[:4].cpu().numpy()
+        spike_rows = torch.nonzero(x.abs().amax(1) > 20000).flatten()[:4].cpu().numpy()
+        picks = np.unique(np.concatenate([picks, zero_rows, spike_rows]))
+        assert float(sdec[torch.as_tensor(zero_rows, device=DEV)].abs().max()) == 0.0
+    _check_sampled(x, codes, scales, sdec, y, picks)
+    assert nv.nvfp4_get_device_status() == 0
+
+
+# ---- edge cases --------------------------------------------------------------------------------
+
+def _edge_matrix(rows, cols, seed):
+    """Rows that hit the corner cases: exact E2M1/E4M3 ties (small multiples of powers of two),
+    zero rows, zero blocks, BF16 subnormals, values near the BF16 maximum, a lone spike,
+    negative values that round to zero, and ordinary Gaussian rows."""
+    rng = np.random.default_rng(seed)
+    x = np.zeros((rows, cols), np.float32)
+    for r in range(rows):
+        kind = r % 8
+        if kind == 0:
+            x[r] = rng.integers(-64, 65, cols) * 2.0 ** rng.integers(-4, 4, cols)
+        elif kind == 1:
+            pass  # zero row
+        elif kind == 2:
+            x[r] = rng.standard_normal(cols)
+            x[r, : min(cols, 16)] = 0.0  # a zero block
+        elif kind == 3:
+            x[r] = rng.standard_normal(cols) * 2.0 ** -130  # BF16 subnormals
+        elif kind == 4:
+            x[r] = rng.standard_normal(cols) * 1e37
+            x[r, 0] = 3.3e38
+        elif kind == 5:
+            x[r] = rng.standard_normal(cols) * 1e-3
+            x[r, rng.integers(cols)] = 3.0e4
+        elif kind == 6:
+            x[r] = -rng.uniform(0, 0.01, cols)
+            x[r, -1] = 6.0
+        else:
+            x[r] = rng.standard_normal(cols) * np.exp(rng.uniform(-20, 20))
+    t = torch.from_numpy(x).to(torch.bfloat16)
+    return t.to(DEV)
+
+
+@pytest.mark.parametrize("cols", [16, 32, 48, 496, 512, 2064, 7168, 7184, 16384, 32768])
+def test_edge_values_and_ragged_widths(cols):
+    rows = 3 if cols >= 16384 else 37
+    x = _edge_matrix(rows, cols, seed=cols)
+    check_rowwise(x)
+    check_rowwise(x, SIX, fused=True, dequant=False)
+    check_tensor(x[: min(rows, 9)].contiguous(), F4)
+
+
+@pytest.mark.parametrize("rows", [1, 2, 7, 31, 33])
+def test_few_rows(rows):
+    check_rowwise(_edge_matrix(rows, 7168, seed=rows))
+
+
+def test_zero_rows_is_noop():
+    x = torch.empty((0, 7168), dtype=torch.bfloat16, device=DEV)
+    codes, scales, sdec = nv.nvfp4_quantize_rowwise(x)
+    assert codes.shape == (0, 3584) and scales.shape == (0, 448) and sdec.shape == (0,)
+    y = nv.nvfp4_dequantize(codes, scales, sdec)
+    assert y.shape == (0, 7168)
+
+
+# ---- determinism and launch independence -------------------------------------------------------
+
+def test_deterministic_and_launch_shape_independent():
+    x = synth.generate(2, device=DEV, rows=1000)["x"]
+    base = [t.clone() for t in nv.nvfp4_fused_roundtrip(x)]
+    shapes = [(1, 1, 0), (1, 2, 1), (3, 1, 5), (8, 2, 0), (2, 4, 17), (0, 0, 3), (7, 3, 0)]
+    try:
+        for w, s, c in shapes:
+            nv.nvfp4_set_launch_config(w, s, c)
+            out = nv.nvfp4_fused_roundtrip(x)
+            for a, b in zip(base, out):
+                assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (w, s, c)
+            t = nv.nvfp4_quantize_tensor(x)
+            assert torch.equal(t[0], nv.nvfp4_quantize_tensor(x)[0])
+    finally:
+        nv.nvfp4_set_launch_config(0, 0, 0)
+    again = nv.nvfp4_fused_roundtrip(x)
+    for a, b in zip(base, again):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+def test_batch_independence_on_gpu():
+    x = synth.generate(3, device=DEV, rows=700)["x"]
+    codes, scales, sdec = nv.nvfp4_quantize_rowwise(x)
+    perm = torch.randperm(x.shape[0], device=DEV, generator=torch.Generator(DEV).manual_seed(1))
+    c2, s2, d2 = nv.nvfp4_quantize_rowwise(x[perm].contiguous())
+    assert torch.equal(c2, codes[perm]) and torch.equal(s2, scales[perm])
+    assert torch.equal(d2, sdec[perm])
+    c3, s3, d3 = nv.nvfp4_quantize_rowwise(x[:123].contiguous())
+    assert torch.equal(c3, codes[:123]) and torch.equal(d3, sdec[:123])
+
+
+def test_streams_are_honoured():
+    x = synth.generate(2, device=DEV, rows=512)["x"]
+    ref = nv.nvfp4_fused_roundtrip(x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = nv.nvfp4_fused_roundtrip(x, stream=s)
+    s.synchronize()
+    for a, b in zip(ref, out):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+# ---- device-side error reporting ---------------------------------------------------------------
+
+def test_group_offsets_validation():
+    d = synth.generate(3, device=DEV, rows=640)
+    x, off = d["x"], d["offsets"]
+    nv.nvfp4_quantize_rowwise(x, group_offsets=off)
+    assert nv.nvfp4_get_device_status() == 0
+    bad = off.clone()
+    bad[5], bad[6] = off[6] + 1, off[5]  # not monotone
+    nv.nvfp4_quantize_rowwise(x, group_offsets=bad)
+    assert nv.nvfp4_get_device_status() == 6
+    short = off.clone()
+    short[-1] = x.shape[0] - 1  # does not end at rows
+    nv.nvfp4_quantize_rowwise(x, group_offsets=short)
+    assert nv.nvfp4_get_device_status() == 6
+    assert nv.nvfp4_get_device_status() == 0  # cleared by the read
+
+
+def test_bounded_wait_reports_timeout():
+    nv.nvfp4_get_device_status(clear=True)
+    nv.nvfp4_selftest_wait_timeout(200_000)  # 0.2 ms on a barrier nobody arrives on
+    assert nv.nvfp4_get_device_status() == 5
+    # The context is still healthy afterwards.
+    check_rowwise(synth.generate(0, device=DEV, rows=16)["x"])
+
+
+def test_host_validation_errors():
+    x = synth.generate(0, device=DEV, rows=4)["x"]
+    with pytest.raises(nv.Nvfp4Error) as e:
+        nv.nvfp4_quantize_rowwise(x[:, :24].contiguous())
+    assert e.value.status == 2
+    with pytest.raises(ValueError):
+        nv.nvfp4_quantize_rowwise(x.cpu())
+    with pytest.raises(nv.Nvfp4Error) as e:
+        nv.nvfp4_quantize_rowwise(torch.empty((4, 65536), dtype=torch.bfloat16, device=DEV))
+    assert e.value.status == 2
