@@ -287,3 +287,13 @@ def test_host_validation_errors():
     with pytest.raises(nv.Nvfp4Error) as e:
         nv.nvfp4_quantize_rowwise(torch.empty((4, 65536), dtype=torch.bfloat16, device=DEV))
     assert e.value.status == 2
+
+
+def test_sharded_tensor_helper_on_one_rank():
+    from nvfp4_block_scaled_row_gb300 import distributed as D
+
+    x = synth.generate(1, device=DEV, rows=256)["x"]
+    want = nv.nvfp4_quantize_tensor(x)
+    got = D.quantize_tensor_sharded(x)
+    for a, b in zip(want, got):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
