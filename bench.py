@@ -315,6 +315,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
+    ap.add_argument("--only", default=None, metavar="WORKLOAD/OP[/KIND[/MODE]]",
+                    help="time one operation on one workload and print one short JSON line "
+                         "(for profiling), e.g. moe_activation/roundtrip or "
+                         "weight_expert_up/quantize/tensor/six")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -334,6 +338,22 @@ def main():
     from nvfp4_block_scaled_row_gb300 import synth
 
     nv.library()
+    if args.only:
+        parts = args.only.split("/")
+        ww = synth.workload(parts[0] if not parts[0].isdigit() else int(parts[0]))
+        op = parts[1]
+        kind = parts[2] if len(parts) > 2 else ww.scale_kind
+        mode = parts[3] if len(parts) > 3 else "four_over_six"
+        d = synth.generate(ww.index, device=device)
+        r = bench_op(nv, d["x"], op, kind, mode, args.steps, args.warmup, world, device,
+                     d["offsets"] if op == "quantize" and kind == "row" else None)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "shape": list(d["x"].shape),
+                              "us_per_step": round(r["ms"] * 1e3, 2), "gbs": round(r["gbs"], 1),
+                              "device_status": nv.nvfp4_get_device_status()}))
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     w = synth.workload(HEADLINE)
     x = synth.generate(HEADLINE, device=device)["x"]
     rows, cols = x.shape
