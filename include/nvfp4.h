@@ -112,6 +112,26 @@ nvfp4_status nvfp4_quantize_tensor_with_amax(const void* x, int64_t rows, int64_
                                              uint8_t* block_scales, float* tensor_scale,
                                              nvfp4_stream_t stream);
 
+/* Per-tensor quantization for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call; it exists for code that must not (or cannot) call cudaMalloc: an
+ * allocator or memory-pool callback, a framework plugin that is handed only its input and output
+ * tensors, or a path where an allocation's implicit synchronization is unacceptable.
+ * Same arguments, outputs and results (bit for bit) as nvfp4_quantize_tensor, minus the
+ * workspace: the partial maxima of the amax pass go to a fixed 2 KB array of device memory
+ * inside the library, held on every GPU that loads the library until the process exits.
+ *   - The first call on each device looks up that array's device address (cudaGetSymbolAddress,
+ *     with the device current) and caches it; make that first call before any stream capture.
+ *   - The array holds at most 512 partial maxima.  The amax pass needs 2 per SM (capped at 1024),
+ *     i.e. 304 on a 152-SM GB300; a device that would need more is refused with
+ *     NVFP4_ERR_WORKSPACE before anything is launched.  Any tensor size is accepted.
+ *   - Every call shares the one array and it keeps the last call's contents; nothing in it has to
+ *     start at zero.  Calls whose kernels overlap on the GPU (different streams with no ordering
+ *     between them) race on the array: order them on one stream. */
+nvfp4_status nvfp4_quantize_tensor_noalloc(const void* x, int64_t rows, int64_t cols,
+                                           nvfp4_mode mode, uint8_t* codes,
+                                           uint8_t* block_scales, float* tensor_scale,
+                                           nvfp4_stream_t stream);
+
 /* Dequantization for the dequantized backward ("NVFP4 RL" Sec. 3):
  * y = bf16_rne(fp32(fp32(q * s) * S_dec)) for every element -- exactly the value the quantizer
  * encoded, rounded once to FP32 and once to BF16.

@@ -18,7 +18,7 @@ from . import build as _build
 __all__ = [
     "Nvfp4Error", "MODE_SIX", "MODE_FOUR_OVER_SIX", "SCALE_ROW", "SCALE_TENSOR",
     "nvfp4_quantize_rowwise", "nvfp4_quantize_tensor", "nvfp4_quantize_tensor_with_amax",
-    "nvfp4_tensor_amax", "nvfp4_dequantize", "nvfp4_fused_roundtrip",
+    "nvfp4_tensor_amax", "nvfp4_quantize_tensor_noalloc", "nvfp4_dequantize", "nvfp4_fused_roundtrip",
     "nvfp4_tensor_workspace_bytes", "nvfp4_get_device_status", "nvfp4_status_string",
     "nvfp4_set_launch_config", "nvfp4_selftest_wait_timeout", "nvfp4_abi_version", "library",
 ]
@@ -67,6 +67,7 @@ def library():
         "nvfp4_quantize_tensor": [P, I64, I64, I, P, P, P, P, SZ, P],
         "nvfp4_tensor_amax": [P, I64, P, P, SZ, P],
         "nvfp4_quantize_tensor_with_amax": [P, I64, I64, I, P, P, P, P, P],
+        "nvfp4_quantize_tensor_noalloc": [P, I64, I64, I, P, P, P, P],
         "nvfp4_dequantize": [P, P, P, I, I64, I64, P, P],
         "nvfp4_fused_roundtrip": [P, I64, I64, I, I, P, P, P, P, P, SZ, P],
         "nvfp4_get_device_status": [I, P],
@@ -211,6 +212,24 @@ def nvfp4_quantize_tensor_with_amax(x, amax, mode="four_over_six", codes=None,
                                                    _ptr(codes), _ptr(block_scales),
                                                    _ptr(tensor_scale), _stream(stream, dev))
     _check(st, "nvfp4_quantize_tensor_with_amax")
+    return codes, block_scales, tensor_scale
+
+
+def nvfp4_quantize_tensor_noalloc(x, mode="four_over_six", codes=None, block_scales=None,
+                                  tensor_scale=None, stream=None):
+    """nvfp4_quantize_tensor without a workspace, for callers that cannot allocate: the amax
+    scratch lives in a fixed device array inside the library.  Outputs that are not supplied are
+    still allocated here; pass them in to keep the call allocation-free.  Calls must not overlap
+    on the GPU (they share the array)."""
+    rows, cols = _input(x)
+    dev = x.device
+    codes = _out(codes, "codes", torch.uint8, (rows, cols // 2), dev)
+    block_scales = _out(block_scales, "block_scales", torch.uint8, (rows, cols // 16), dev)
+    tensor_scale = _out(tensor_scale, "tensor_scale", torch.float32, (1,), dev)
+    st = library().nvfp4_quantize_tensor_noalloc(_ptr(x), rows, cols, _MODES[mode], _ptr(codes),
+                                                 _ptr(block_scales), _ptr(tensor_scale),
+                                                 _stream(stream, dev))
+    _check(st, "nvfp4_quantize_tensor_noalloc")
     return codes, block_scales, tensor_scale
 
 

@@ -167,6 +167,29 @@ cudaError_t launch_amax_partials(const uint16_t* x, int64_t n, float* partials, 
   return cudaGetLastError();
 }
 
+cudaError_t launch_amax_partials_into(const uint16_t* x, int64_t n, float* partials, int capacity,
+                                      int* n_partials, bool* too_small, cudaStream_t stream) {
+  *too_small = false;
+  int device = 0;
+  cudaError_t err = cudaGetDevice(&device);
+  if (err != cudaSuccess) return err;
+  const int64_t per_cta = static_cast<int64_t>(kAmaxThreads) * 8 * kAmaxUnroll;
+  int64_t grid = (n + per_cta - 1) / per_cta;
+  int64_t cap = static_cast<int64_t>(sm_count(device)) * 2;
+  if (cap > kAmaxMaxPartials) cap = kAmaxMaxPartials;
+  if (grid > cap) grid = cap;
+  const LaunchOverride ov = launch_override();
+  if (ov.max_ctas > 0 && grid > ov.max_ctas) grid = ov.max_ctas;
+  if (grid < 1) grid = 1;
+  if (grid > capacity) {
+    *too_small = true;
+    return cudaSuccess;
+  }
+  amax_partials_kernel<<<static_cast<unsigned>(grid), kAmaxThreads, 0, stream>>>(x, n, partials);
+  *n_partials = static_cast<int>(grid);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_amax_finalize(const float* partials, int n, float* out, cudaStream_t stream) {
   amax_finalize_kernel<<<1, 256, 0, stream>>>(partials, n, out);
   return cudaGetLastError();

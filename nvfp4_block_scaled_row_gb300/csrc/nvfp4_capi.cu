@@ -130,6 +130,15 @@ nvfp4_status run_tensor(const void* x, int64_t rows, int64_t cols, int mode, uin
 
 }  // namespace
 
+int check_tensor_quantize_args(const void* x, int64_t rows, int64_t cols, int mode,
+                               const uint8_t* codes, const uint8_t* block_scales,
+                               const float* tensor_scale, bool* noop) {
+  return check_quantize(x, rows, cols, mode, codes, block_scales, tensor_scale, true, nullptr,
+                        false, noop);
+}
+
+cudaError_t device_status_word(int** out) { return status_ptr(out); }
+
 LaunchOverride launch_override() {
   return {g_override_warps.load(), g_override_stages.load(), g_override_max_ctas.load()};
 }

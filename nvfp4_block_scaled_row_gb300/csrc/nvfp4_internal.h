@@ -39,4 +39,18 @@ cudaError_t launch_amax_finalize(const float* partials, int n, float* out, cudaS
 
 cudaError_t launch_wait_timeout_selftest(int* status, uint64_t timeout_ns, cudaStream_t stream);
 
+// As launch_amax_partials, but into a fixed-capacity buffer: sets *too_small and launches
+// nothing when the partial maxima would not fit in `capacity` floats.
+cudaError_t launch_amax_partials_into(const uint16_t* x, int64_t n, float* partials, int capacity,
+                                      int* n_partials, bool* too_small, cudaStream_t stream);
+
+// Host-side argument checks of the per-tensor quantize calls (the rules nvfp4_quantize_tensor
+// applies, without the workspace); *noop is set for rows == 0.
+int check_tensor_quantize_args(const void* x, int64_t rows, int64_t cols, int mode,
+                               const uint8_t* codes, const uint8_t* block_scales,
+                               const float* tensor_scale, bool* noop);
+
+// Device address of the status word on the current device.
+cudaError_t device_status_word(int** out);
+
 }  // namespace nvfp4
