@@ -297,7 +297,7 @@ const char* nvfp4_status_string(nvfp4_status status) {
 }
 
 nvfp4_status nvfp4_set_launch_config(int warps_per_cta, int stages, int max_ctas) {
-  if (warps_per_cta < 0 || warps_per_cta > 8 || stages < 0 || stages > kMaxStages ||
+  if (warps_per_cta < 0 || warps_per_cta > kMaxWarpsPerCta || stages < 0 || stages > kMaxStages ||
       max_ctas < 0)
     return NVFP4_ERR_INVALID_ARG;
   g_override_warps.store(warps_per_cta);

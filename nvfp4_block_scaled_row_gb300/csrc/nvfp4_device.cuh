@@ -15,11 +15,19 @@ namespace nvfp4 {
 
 constexpr int kBlockElems = 16;          // elements per E4M3-scaled block
 constexpr int kMaxCols = 32768;          // widest row the shared-memory ring supports
-constexpr int kMaxWarpsPerCta = 8;
-constexpr int kMaxStages = 8;
-constexpr int kTableBytes = 256 * 16;    // one ScaleEntry per E4M3 byte
-constexpr int kBarrierBytes = kMaxWarpsPerCta * kMaxStages * 8;
+constexpr int kMaxWarpsPerCta = 16;
+constexpr int kMaxStages = 4;
+constexpr int kMaxTeam = 8;              // warps that share one row
+constexpr int kMaxBlocksPerLane = 8;     // 16-element blocks one lane owns per row (<= 8 KB slots)
 constexpr int kAmaxMaxPartials = 1024;   // per-tensor amax: partial maxima in the workspace
+
+// Shared-memory header of the quantize kernel, then the ring (128-byte aligned).
+constexpr int kTableBytes = 256 * 8;                          // one ScaleEntry per E4M3 byte
+constexpr int kXchBytes = 2 * kMaxWarpsPerCta * 4;            // row-amax partials, 2 parities
+constexpr int kAbortBytes = kMaxWarpsPerCta * 4;              // per-team abort flags
+constexpr int kBarrierBytes = kMaxWarpsPerCta * kMaxStages * 8;
+constexpr int kHeaderBytes =
+    ((kTableBytes + kXchBytes + kAbortBytes + kBarrierBytes + 127) / 128) * 128;
 
 // Device status codes (same numbers as nvfp4_status in include/nvfp4.h).
 constexpr int kStatusTimeout = 5;
@@ -29,13 +37,11 @@ constexpr int kStatusOffsets = 6;
 constexpr int kModeSix = 0;
 constexpr int kModeFourOverSix = 1;
 
-// Per E4M3 byte: the scale s, its correctly rounded reciprocal (0 for s == 0), and -s and +s as
-// FP16 pairs (E4M3 values are exact in FP16).
-struct __align__(16) ScaleEntry {
-  float s;
+// Per E4M3 byte: the correctly rounded reciprocal of its value s (0 for s == 0) and -s as an
+// FP16 pair (E4M3 values are exact in FP16).
+struct __align__(8) ScaleEntry {
   float inv;
   uint32_t neg_s_h2;
-  uint32_t s_h2;
 };
 
 struct QuantParams {
@@ -51,7 +57,9 @@ struct QuantParams {
   const int32_t* offsets;   // optional group offsets [num_groups + 1]
   int32_t num_groups;
   int32_t stages;           // ring slots per warp
-  uint32_t slot_bytes;      // bytes per ring slot (>= 2*cols, multiple of 128)
+  int32_t team;             // warps sharing one row
+  int32_t blocks_per_warp;  // 16-element blocks each warp of a team owns
+  uint32_t slot_bytes;      // bytes per ring slot (>= 32 * blocks_per_warp, multiple of 128)
   int* status;              // device status word
   uint64_t timeout_ns;      // bound on every barrier wait
 };
@@ -177,6 +185,19 @@ __device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) {
   return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+// Two BF16 values widened to an FP32 pair on the FMA pipe: x * 1 + (-0) with BF16 operands and
+// an FP32 result is exact and keeps the sign of zero (same result as bf16x2_to_f32x2).
+__device__ __forceinline__ f32x2 bf16x2_to_f32x2_fma(uint32_t w, uint16_t one_bf16, float neg_zero) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, l, %3, %4;\n\t"
+      "fma.rn.f32.bf16 %1, h, %3, %4;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w), "h"(one_bf16), "f"(neg_zero));
+  return pack2(lo, hi);
+}
+
 // ------------------------------------------------------------------------------------------------
 // Format conversions (hardware, round-to-nearest-even, saturating where named)
 // ------------------------------------------------------------------------------------------------
@@ -230,6 +251,33 @@ __device__ __forceinline__ uint32_t e2m1x8_from_f32x2(f32x2 p0, f32x2 p1, f32x2 
   return w;
 }
 
+// Eight FP32 targets (four pairs, element 2j in .x) rounded to E2M1 (RNE, satfinite, sign kept)
+// and decoded back, in one step: returns the packed code word (element i in nibble i) and the
+// four decoded FP16 pairs (element 2j in the low half).  The code bytes stay in registers between
+// the two conversions.
+__device__ __forceinline__ uint32_t e2m1x8_encode_decode(f32x2 p0, f32x2 p1, f32x2 p2, f32x2 p3,
+                                                        uint32_t (&h)[4]) {
+  float a0, a1, b0, b1, c0, c1, d0, d1;
+  unpack2(p0, a0, a1);
+  unpack2(p1, b0, b1);
+  unpack2(p2, c0, c1);
+  unpack2(p3, d0, d1);
+  uint32_t w;
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %8, %7;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %10, %9;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %12, %11;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, q0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, q1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, q2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %4, q3;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+      : "=r"(w), "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1), "f"(d0), "f"(d1));
+  return w;
+}
+
 // Eight E2M1 codes (nibble i = element i) to four FP16 pairs (element 2j in the low half).
 __device__ __forceinline__ void f16x2_from_e2m1x8(uint32_t w, uint32_t (&h)[4]) {
   asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
@@ -270,11 +318,14 @@ __device__ __forceinline__ ScaleEntry make_scale_entry(uint32_t byte) {
   const uint32_t h2 = f16x2_from_e4m3x2(byte | (byte << 8));  // (s, s) in FP16
   const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
   ScaleEntry e;
-  e.s = s;
   e.inv = (s == 0.0f || !(s == s)) ? 0.0f : __frcp_rn(s);
-  e.s_h2 = h2;
   e.neg_s_h2 = h2 ^ 0x80008000u;
   return e;
+}
+
+// Named barrier over `threads` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 }  // namespace nvfp4

@@ -64,15 +64,13 @@ __device__ __forceinline__ Candidate encode_candidate(const f32x2 (&z)[8], const
   f32x2 t[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) t[j] = mul2(z[j], inv2);  // target scaled down by 1/s
-  c.cw[0] = e2m1x8_from_f32x2(t[0], t[1], t[2], t[3]);
-  c.cw[1] = e2m1x8_from_f32x2(t[4], t[5], t[6], t[7]);
   uint32_t rA[4], rB[4];
-  f16x2_from_e2m1x8(c.cw[0], rA);
-  f16x2_from_e2m1x8(c.cw[1], rB);
+  c.cw[0] = e2m1x8_encode_decode(t[0], t[1], t[2], t[3], rA);
+  c.cw[1] = e2m1x8_encode_decode(t[4], t[5], t[6], t[7], rB);
   f32x2 accA = pack2(0.0f, 0.0f), accB = pack2(0.0f, 0.0f);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const f32x2 dA = fma_f16x2_f32x2(rA[j], e.neg_s_h2, z[j]);      // z - r*s, one rounding
+    const f32x2 dA = fma_f16x2_f32x2(rA[j], e.neg_s_h2, z[j]);  // z - r*s, one rounding
     const f32x2 dB = fma_f16x2_f32x2(rB[j], e.neg_s_h2, z[4 + j]);
     accA = fma2(dA, dA, accA);
     accB = fma2(dB, dB, accB);
@@ -86,21 +84,36 @@ __device__ __forceinline__ Candidate encode_candidate(const f32x2 (&z)[8], const
   return c;
 }
 
+// Shared-memory layout: [table | amax exchange | abort flags | barriers] (kHeaderBytes), then the
+// ring: warp w owns `stages` slots of `slot_bytes`.
+//
+// Work split: a team of `team` warps shares each row; warp t of a team owns the blocks
+// [t*bpw, min(nblk, (t+1)*bpw)) and stages only that part of the row.  Teams take rows
+// gt, gt + NT, gt + 2NT, ... (gt = global team index, NT = number of teams).  With more than one
+// warp per team the row amax is combined through shared memory behind a named barrier; if any
+// member's copy times out, all members leave together after that barrier.
 template <int kMode, bool kTensor, bool kFused>
-__global__ void __launch_bounds__(256, 1) quantize_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const QuantParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   ScaleEntry* tab = reinterpret_cast<ScaleEntry*>(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTableBytes);
-  unsigned char* ring = smem + kTableBytes + kBarrierBytes;
+  float* xch = reinterpret_cast<float*>(smem + kTableBytes);
+  int* abort_flag = reinterpret_cast<int*>(smem + kTableBytes + kXchBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTableBytes + kXchBytes + kAbortBytes);
+  unsigned char* ring = smem + kHeaderBytes;
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
   const int S = p.stages;
+  const int TW = p.team;
+  const int teams = nwarps / TW;
+  const int team = warp / TW;
+  const int tw = warp - team * TW;
   uint64_t* my_bars = bars + warp * S;
   unsigned char* my_ring = ring + static_cast<size_t>(warp) * S * p.slot_bytes;
 
   for (int i = threadIdx.x; i < 256; i += blockDim.x) tab[i] = make_scale_entry(i);
+  if (threadIdx.x < kMaxWarpsPerCta) abort_flag[threadIdx.x] = 0;
   if (lane == 0)
     for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
   fence_barrier_init();
@@ -120,9 +133,12 @@ __global__ void __launch_bounds__(256, 1) quantize_kernel(const QuantParams p) {
 
   const int cols = p.cols;
   const int nblk = cols / kBlockElems;
-  const uint32_t row_bytes = static_cast<uint32_t>(cols) * 2u;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
-  const int64_t NW = static_cast<int64_t>(gridDim.x) * nwarps;
+  const int b0 = tw * p.blocks_per_warp;
+  const int b1 = min(nblk, b0 + p.blocks_per_warp);
+  const bool has_work = b1 > b0;
+  const uint32_t chunk_bytes = has_work ? static_cast<uint32_t>(b1 - b0) * 32u : 0u;
+  const int64_t gt = static_cast<int64_t>(blockIdx.x) * teams + team;
+  const int64_t NT = static_cast<int64_t>(gridDim.x) * teams;
   const uint64_t policy = l2_evict_first_policy();
   const int h0 = (lane >> 2) & 1;  // which 16-byte half of its block this lane reads first
 
@@ -136,65 +152,101 @@ __global__ void __launch_bounds__(256, 1) quantize_kernel(const QuantParams p) {
     if (blockIdx.x == 0 && threadIdx.x == 0) p.scale_out[0] = f.S_dec;
   }
 
-  // Prologue: fill the ring.
+  // Prologue: fill the ring with this warp's part of the team's first rows.
   int64_t issued = 0;
-  if (lane == 0) {
+  if (lane == 0 && has_work) {
     for (int s = 0; s < S; ++s) {
-      const int64_t row = gw + s * NW;
+      const int64_t row = gt + s * NT;
       if (row >= p.rows) break;
-      mbar_arrive_expect_tx(&my_bars[s], row_bytes);
-      bulk_load(my_ring + static_cast<size_t>(s) * p.slot_bytes, p.x + row * cols, row_bytes,
-                &my_bars[s], policy);
+      mbar_arrive_expect_tx(&my_bars[s], chunk_bytes);
+      bulk_load(my_ring + static_cast<size_t>(s) * p.slot_bytes, p.x + row * cols + b0 * 16,
+                chunk_bytes, &my_bars[s], policy);
       ++issued;
     }
   }
 
   int64_t k = 0;
-  for (int64_t row = gw; row < p.rows; row += NW, ++k) {
+  for (int64_t row = gt; row < p.rows; row += NT, ++k) {
     const int slot = static_cast<int>(k % S);
     const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
     int ok = 1;
-    if (lane == 0) ok = mbar_wait_bounded(&my_bars[slot], parity, p.timeout_ns) ? 1 : 0;
+    if (lane == 0 && has_work) ok = mbar_wait_bounded(&my_bars[slot], parity, p.timeout_ns) ? 1 : 0;
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) {
-      // A copy did not land in time: record it, give the copies still in flight one more
-      // bounded wait so none lands after this warp is gone, and stop.
-      if (lane == 0) {
-        record_status(p.status, kStatusTimeout);
+    const bool team_sync = !kTensor && TW > 1;
+    if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
+    if (!ok && !team_sync) {
+      // A copy did not land in time: give the copies still in flight one more bounded wait so
+      // none lands after this warp is gone, and stop.
+      if (lane == 0)
         for (int64_t i = k; i < issued; ++i)
           (void)mbar_wait_bounded(&my_bars[i % S], static_cast<uint32_t>((i / S) & 1),
                                   p.timeout_ns);
-      }
       return;
     }
     const unsigned char* xs = my_ring + static_cast<size_t>(slot) * p.slot_bytes;
 
+    // Pass 1 (row scale): block maxima (kept in registers for pass 2) and the row amax.
+    uint32_t bmax[kMaxBlocksPerLane];
     if (!kTensor) {
-      // Pass 1: row amax.
       uint32_t m2 = 0;
-      for (int b = lane; b < nblk; b += 32) {
-        const uint4 A = *reinterpret_cast<const uint4*>(xs + b * 32 + h0 * 16);
-        const uint4 B = *reinterpret_cast<const uint4*>(xs + b * 32 + (1 - h0) * 16);
-        m2 = max_abs_bf16x2(m2, max_abs_bf16x2(max_abs_bf16x2(A.x, A.y), max_abs_bf16x2(A.z, A.w)));
-        m2 = max_abs_bf16x2(m2, max_abs_bf16x2(max_abs_bf16x2(B.x, B.y), max_abs_bf16x2(B.z, B.w)));
+#pragma unroll
+      for (int j = 0; j < kMaxBlocksPerLane; ++j) {
+        const int b = b0 + lane + 32 * j;
+        bmax[j] = 0;
+        if (ok && b < b1) {
+          const unsigned char* blk = xs + (b - b0) * 32;
+          const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
+          const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
+          bmax[j] = max_abs_bf16x2(
+              max_abs_bf16x2(max_abs_bf16x2(A.x, A.y), max_abs_bf16x2(A.z, A.w)),
+              max_abs_bf16x2(max_abs_bf16x2(B.x, B.y), max_abs_bf16x2(B.z, B.w)));
+          m2 = max_abs_bf16x2(m2, bmax[j]);
+        }
       }
       float a = abs_max_of_pair(m2);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+      if (team_sync) {
+        float* part = xch + (k & 1) * kMaxWarpsPerCta;
+        if (lane == 0) {
+          part[warp] = a;
+          if (!ok) abort_flag[team] = 1;
+        }
+        named_barrier(1 + team, TW * 32);
+        if (abort_flag[team]) {
+          if (lane == 0)
+            for (int64_t i = k; i < issued; ++i)
+              (void)mbar_wait_bounded(&my_bars[i % S], static_cast<uint32_t>((i / S) & 1),
+                                      p.timeout_ns);
+          return;
+        }
+        a = 0.0f;
+        for (int j = 0; j < TW; ++j) a = fmaxf(a, part[team * TW + j]);
+      }
       f = row_factors<kMode>(a);
-      if (lane == 0) p.scale_out[row] = f.S_dec;
+      if (lane == 0 && tw == 0) p.scale_out[row] = f.S_dec;
     }
 
-    // Pass 2: encode.
+    // Pass 2: encode this warp's blocks.
     const f32x2 senc2 = pack2(f.S_enc, f.S_enc);
+    const uint16_t one_bf16 = 0x3F80;
+    const float neg_zero = -0.0f;
     uint8_t* codes_row = p.codes + row * (cols / 2);
     uint8_t* scales_row = p.scales + row * nblk;
-    for (int b = lane; b < nblk; b += 32) {
-      const uint4 A = *reinterpret_cast<const uint4*>(xs + b * 32 + h0 * 16);
-      const uint4 B = *reinterpret_cast<const uint4*>(xs + b * 32 + (1 - h0) * 16);
-      const uint32_t mx = max_abs_bf16x2(
-          max_abs_bf16x2(max_abs_bf16x2(A.x, A.y), max_abs_bf16x2(A.z, A.w)),
-          max_abs_bf16x2(max_abs_bf16x2(B.x, B.y), max_abs_bf16x2(B.z, B.w)));
+#pragma unroll
+    for (int j = 0; j < kMaxBlocksPerLane; ++j) {
+      const int b = b0 + lane + 32 * j;
+      if (b >= b1) break;
+      const unsigned char* blk = xs + (b - b0) * 32;
+      const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
+      const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
+      uint32_t mx;
+      if (kTensor) {
+        mx = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(A.x, A.y), max_abs_bf16x2(A.z, A.w)),
+                            max_abs_bf16x2(max_abs_bf16x2(B.x, B.y), max_abs_bf16x2(B.z, B.w)));
+      } else {
+        mx = bmax[j];
+      }
       const float m = abs_max_of_pair(mx);
       const float u6 = __fmul_rn(m, f.c6);
       const float u4 = (kMode == kModeFourOverSix) ? __fmul_rn(m, f.c4) : 0.0f;
@@ -202,14 +254,14 @@ __global__ void __launch_bounds__(256, 1) quantize_kernel(const QuantParams p) {
       const uint32_t b6 = sb & 0xFFu, b4 = sb >> 8;
 
       f32x2 z[8];
-      z[0] = mul2(bf16x2_to_f32x2(A.x), senc2);
-      z[1] = mul2(bf16x2_to_f32x2(A.y), senc2);
-      z[2] = mul2(bf16x2_to_f32x2(A.z), senc2);
-      z[3] = mul2(bf16x2_to_f32x2(A.w), senc2);
-      z[4] = mul2(bf16x2_to_f32x2(B.x), senc2);
-      z[5] = mul2(bf16x2_to_f32x2(B.y), senc2);
-      z[6] = mul2(bf16x2_to_f32x2(B.z), senc2);
-      z[7] = mul2(bf16x2_to_f32x2(B.w), senc2);
+      z[0] = mul2(bf16x2_to_f32x2_fma(A.x, one_bf16, neg_zero), senc2);
+      z[1] = mul2(bf16x2_to_f32x2_fma(A.y, one_bf16, neg_zero), senc2);
+      z[2] = mul2(bf16x2_to_f32x2_fma(A.z, one_bf16, neg_zero), senc2);
+      z[3] = mul2(bf16x2_to_f32x2_fma(A.w, one_bf16, neg_zero), senc2);
+      z[4] = mul2(bf16x2_to_f32x2_fma(B.x, one_bf16, neg_zero), senc2);
+      z[5] = mul2(bf16x2_to_f32x2_fma(B.y, one_bf16, neg_zero), senc2);
+      z[6] = mul2(bf16x2_to_f32x2_fma(B.z, one_bf16, neg_zero), senc2);
+      z[7] = mul2(bf16x2_to_f32x2_fma(B.w, one_bf16, neg_zero), senc2);
 
       const ScaleEntry e6 = tab[b6];
       const Candidate c6 = encode_candidate(z, e6);
@@ -227,7 +279,7 @@ __global__ void __launch_bounds__(256, 1) quantize_kernel(const QuantParams p) {
       scales_row[b] = static_cast<uint8_t>(pick4 ? b4 : b6);
 
       if (kFused) {
-        const uint32_t s_h2 = pick4 ? e4.s_h2 : e6.s_h2;
+        const uint32_t s_h2 = (pick4 ? e4.neg_s_h2 : e6.neg_s_h2) ^ 0x80008000u;
         const f32x2 sdec2 = pack2(f.S_dec, f.S_dec);
         const f32x2 nzero = pack2(-0.0f, -0.0f);
         uint32_t out[8];
@@ -243,14 +295,14 @@ __global__ void __launch_bounds__(256, 1) quantize_kernel(const QuantParams p) {
       }
     }
 
-    // Slot consumed: refill it with the row `stages` steps ahead.
+    // Slot consumed: refill it with this warp's part of the row `stages` steps ahead.
     __syncwarp();
-    if (lane == 0) {
-      const int64_t next = row + static_cast<int64_t>(S) * NW;
+    if (lane == 0 && has_work) {
+      const int64_t next = row + static_cast<int64_t>(S) * NT;
       if (next < p.rows) {
-        mbar_arrive_expect_tx(&my_bars[slot], row_bytes);
-        bulk_load(my_ring + static_cast<size_t>(slot) * p.slot_bytes, p.x + next * cols, row_bytes,
-                  &my_bars[slot], policy);
+        mbar_arrive_expect_tx(&my_bars[slot], chunk_bytes);
+        bulk_load(my_ring + static_cast<size_t>(slot) * p.slot_bytes, p.x + next * cols + b0 * 16,
+                  chunk_bytes, &my_bars[slot], policy);
         ++issued;
       }
     }
@@ -260,31 +312,46 @@ __global__ void __launch_bounds__(256, 1) quantize_kernel(const QuantParams p) {
 struct RingShape {
   int warps;
   int stages;
+  int team;
+  int blocks_per_warp;
   uint32_t slot_bytes;
   size_t smem;
 };
 
 constexpr size_t kSmemLimit = 227 * 1024;
-constexpr int kDefaultWarps = 8;
+constexpr uint32_t kTargetSlotBytes = 8192;  // split rows wider than this across a team
 
+// Team size, ring depth and warps per CTA for rows of `cols` elements: as many warps as shared
+// memory allows (up to 16), then as many stages as fit (up to 4, at least 2 when possible).
 bool choose_ring(int64_t cols, RingShape* out) {
-  const uint32_t slot = static_cast<uint32_t>(((cols * 2 + 127) / 128) * 128);
-  const size_t avail = kSmemLimit - kTableBytes - kBarrierBytes;
+  if (cols <= 0 || cols % kBlockElems != 0 || cols > kMaxCols) return false;
+  const int nblk = static_cast<int>(cols / kBlockElems);
+  int team = 1;
+  while (team < kMaxTeam && ((nblk + team - 1) / team) * 32u > kTargetSlotBytes) team *= 2;
+  while (team > 1 && (team - 1) * ((nblk + team - 1) / team) >= nblk) team /= 2;
+  const int bpw = (nblk + team - 1) / team;
+  const uint32_t slot = static_cast<uint32_t>(((bpw * 32 + 127) / 128) * 128);
+  const size_t avail = kSmemLimit - kHeaderBytes;
   const LaunchOverride ov = launch_override();
-  int stages = ov.stages > 0 ? ov.stages : (slot <= 4096 ? 4 : (slot <= 8192 ? 3 : 2));
-  int warps = 0;
-  for (; stages >= 1; --stages) {
-    warps = static_cast<int>(avail / (static_cast<size_t>(stages) * slot));
-    if (warps >= 1) break;
+  int max_warps = kMaxWarpsPerCta;
+  if (ov.warps_per_cta > 0) max_warps = ov.warps_per_cta < team ? team : ov.warps_per_cta;
+  max_warps -= max_warps % team;
+  for (int min_stages : {2, 1}) {
+    for (int warps = max_warps; warps >= team; warps -= team) {
+      for (int stages = kMaxStages; stages >= min_stages; --stages) {
+        if (ov.stages > 0 && stages != ov.stages) continue;
+        if (static_cast<size_t>(warps) * stages * slot > avail) continue;
+        out->warps = warps;
+        out->stages = stages;
+        out->team = team;
+        out->blocks_per_warp = bpw;
+        out->slot_bytes = slot;
+        out->smem = kHeaderBytes + static_cast<size_t>(warps) * stages * slot;
+        return true;
+      }
+    }
   }
-  if (stages < 1 || warps < 1) return false;
-  warps = warps < kDefaultWarps ? warps : kDefaultWarps;
-  if (ov.warps_per_cta > 0 && ov.warps_per_cta < warps) warps = ov.warps_per_cta;
-  out->warps = warps;
-  out->stages = stages;
-  out->slot_bytes = slot;
-  out->smem = kTableBytes + kBarrierBytes + static_cast<size_t>(warps) * stages * slot;
-  return true;
+  return false;
 }
 
 template <int kMode, bool kTensor, bool kFused>
@@ -301,13 +368,16 @@ cudaError_t launch_impl(QuantParams p, cudaStream_t stream) {
   err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, rs.warps * 32, rs.smem);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
-  int64_t grid = (p.rows + rs.warps - 1) / rs.warps;
+  const int teams = rs.warps / rs.team;
+  int64_t grid = (p.rows + teams - 1) / teams;
   const int64_t cap = static_cast<int64_t>(sm_count(device)) * per_sm;
   if (grid > cap) grid = cap;
   const LaunchOverride ov = launch_override();
   if (ov.max_ctas > 0 && grid > ov.max_ctas) grid = ov.max_ctas;
   if (grid < 1) grid = 1;
   p.stages = rs.stages;
+  p.team = rs.team;
+  p.blocks_per_warp = rs.blocks_per_warp;
   p.slot_bytes = rs.slot_bytes;
   kern<<<static_cast<unsigned>(grid), rs.warps * 32, rs.smem, stream>>>(p);
   return cudaGetLastError();

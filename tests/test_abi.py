@@ -120,7 +120,8 @@ def test_dequantize_host_validation(lib):
 def test_launch_config_validation(lib):
     assert lib.nvfp4_set_launch_config(-1, 0, 0) == INVALID
     assert lib.nvfp4_set_launch_config(0, 99, 0) == INVALID
-    assert lib.nvfp4_set_launch_config(9, 0, 0) == INVALID
+    assert lib.nvfp4_set_launch_config(17, 0, 0) == INVALID
+    assert lib.nvfp4_set_launch_config(0, 5, 0) == INVALID
     assert lib.nvfp4_set_launch_config(2, 2, 5) == OK
     assert lib.nvfp4_set_launch_config(0, 0, 0) == OK
 
