@@ -14,6 +14,7 @@
 // keeps every 128-bit shared-memory read free of bank conflicts.  The errors are summed in the
 // fixed order the spec prescribes (four FMA chains, then a pairwise combine), so the result is
 // bit-identical to the CPU oracle and independent of the launch shape.
+#include <atomic>
 #include <cfloat>
 
 #include "nvfp4_device.cuh"
@@ -44,6 +45,24 @@ __device__ __forceinline__ RowFactors row_factors(float a) {
   f.c6 = fminf(__fdiv_rn(M, a), FLT_MAX);
   f.c4 = fminf(__fdiv_rn(1.5f * M, a), FLT_MAX);
   f.S_dec = __fdiv_rn(a, 6.0f * M);
+  return f;
+}
+
+// The same four factors for a warp-uniform amax `a`, each division done once by its own lane
+// (lanes 0-3) and broadcast; identical results to row_factors.
+template <int kMode>
+__device__ __forceinline__ RowFactors row_factors_warp(float a, int lane) {
+  constexpr float M = (kMode == kModeFourOverSix) ? 256.0f : 448.0f;
+  const float num = lane == 0 ? 6.0f * M : (lane == 1 ? M : (lane == 2 ? 1.5f * M : a));
+  const float den = lane == 3 ? 6.0f * M : a;
+  float q = __fdiv_rn(num, den);
+  if (lane < 3) q = fminf(q, FLT_MAX);
+  RowFactors f;
+  f.S_enc = __shfl_sync(0xFFFFFFFFu, q, 0);
+  f.c6 = __shfl_sync(0xFFFFFFFFu, q, 1);
+  f.c4 = __shfl_sync(0xFFFFFFFFu, q, 2);
+  f.S_dec = __shfl_sync(0xFFFFFFFFu, q, 3);
+  if (a == 0.0f) f.S_enc = f.c6 = f.c4 = f.S_dec = 0.0f;
   return f;
 }
 
@@ -154,16 +173,14 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
 
   // Prologue: fill the ring with this warp's part of the team's first rows.
   int64_t issued = 0;
-  if (lane == 0 && has_work) {
-    for (int s = 0; s < S; ++s) {
-      const int64_t row = gt + s * NT;
-      if (row >= p.rows) break;
-      mbar_arrive_expect_tx(&my_bars[s], chunk_bytes);
-      bulk_load(my_ring + static_cast<size_t>(s) * p.slot_bytes, p.x + row * cols + b0 * 16,
-                chunk_bytes, &my_bars[s], policy);
-      ++issued;
-    }
-  }
+  auto issue = [&](int slot_index, int64_t row) {
+    mbar_arrive_expect_tx(&my_bars[slot_index], chunk_bytes);
+    bulk_load(my_ring + static_cast<size_t>(slot_index) * p.slot_bytes, p.x + row * cols + b0 * 16,
+              chunk_bytes, &my_bars[slot_index], policy);
+    ++issued;
+  };
+  if (lane == 0 && has_work)
+    for (int s = 0; s < S && gt + s * NT < p.rows; ++s) issue(s, gt + s * NT);
 
   int64_t k = 0;
   for (int64_t row = gt; row < p.rows; row += NT, ++k) {
@@ -223,7 +240,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
         a = 0.0f;
         for (int j = 0; j < TW; ++j) a = fmaxf(a, part[team * TW + j]);
       }
-      f = row_factors<kMode>(a);
+      f = row_factors_warp<kMode>(a, lane);
       if (lane == 0 && tw == 0) p.scale_out[row] = f.S_dec;
     }
 
@@ -247,7 +264,9 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
       } else {
         mx = bmax[j];
       }
-      const float m = abs_max_of_pair(mx);
+      // Both halves of `mm` hold the block's largest |x| (sign bits arbitrary; fabsf drops them).
+      const uint32_t mm = max_abs_bf16x2(mx, __byte_perm(mx, 0, 0x1032));
+      const float m = fabsf(__uint_as_float(mm << 16));
       const float u6 = __fmul_rn(m, f.c6);
       const float u4 = (kMode == kModeFourOverSix) ? __fmul_rn(m, f.c4) : 0.0f;
       const uint32_t sb = e4m3x2_from_f32(u4, u6);
@@ -275,7 +294,9 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
       }
       const uint32_t wA = pick4 ? c4.cw[0] : c6.cw[0];
       const uint32_t wB = pick4 ? c4.cw[1] : c6.cw[1];
-      *reinterpret_cast<uint2*>(codes_row + b * 8) = h0 ? make_uint2(wB, wA) : make_uint2(wA, wB);
+      uint32_t* cw = reinterpret_cast<uint32_t*>(codes_row + b * 8);
+      cw[h0] = wA;  // half A holds elements 8*h0 .. 8*h0+7 of the block
+      cw[1 - h0] = wB;
       scales_row[b] = static_cast<uint8_t>(pick4 ? b4 : b6);
 
       if (kFused) {
@@ -299,12 +320,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
     __syncwarp();
     if (lane == 0 && has_work) {
       const int64_t next = row + static_cast<int64_t>(S) * NT;
-      if (next < p.rows) {
-        mbar_arrive_expect_tx(&my_bars[slot], chunk_bytes);
-        bulk_load(my_ring + static_cast<size_t>(slot) * p.slot_bytes, p.x + next * cols + b0 * 16,
-                  chunk_bytes, &my_bars[slot], policy);
-        ++issued;
-      }
+      if (next < p.rows) issue(slot, next);
     }
   }
 }
@@ -354,20 +370,57 @@ bool choose_ring(int64_t cols, RingShape* out) {
   return false;
 }
 
+// Per kernel instantiation and device: whether the shared-memory limit has been raised, and the
+// resident CTAs per SM for each launch shape seen (looked up once, then reused).
+struct LaunchCache {
+  static constexpr int kDevices = 64;
+  static constexpr int kShapes = 8;
+  std::atomic<int> attr_set[kDevices];
+  struct Entry {
+    std::atomic<long long> key;  // warps | stages << 8 | slot_bytes << 16, 0 = empty
+    std::atomic<int> per_sm;
+  } entries[kDevices][kShapes];
+};
+
 template <int kMode, bool kTensor, bool kFused>
 cudaError_t launch_impl(QuantParams p, cudaStream_t stream) {
+  static LaunchCache cache;
   RingShape rs;
   if (!choose_ring(p.cols, &rs)) return cudaErrorInvalidValue;
   auto kern = quantize_kernel<kMode, kTensor, kFused>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemLimit));
-  if (err != cudaSuccess) return err;
   int device = 0;
-  if ((err = cudaGetDevice(&device)) != cudaSuccess) return err;
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, rs.warps * 32, rs.smem);
+  cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
-  if (per_sm < 1) per_sm = 1;
+  const bool cached_dev = device >= 0 && device < LaunchCache::kDevices;
+  if (!cached_dev || cache.attr_set[device].load() == 0) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemLimit));
+    if (err != cudaSuccess) return err;
+    if (cached_dev) cache.attr_set[device].store(1);
+  }
+  const long long key = static_cast<long long>(rs.warps) | (static_cast<long long>(rs.stages) << 8) |
+                        (static_cast<long long>(rs.slot_bytes) << 16);
+  int per_sm = 0;
+  if (cached_dev)
+    for (auto& e : cache.entries[device])
+      if (e.key.load() == key) {
+        per_sm = e.per_sm.load();
+        break;
+      }
+  if (per_sm == 0) {
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, rs.warps * 32, rs.smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    if (cached_dev)
+      for (auto& e : cache.entries[device]) {
+        long long empty = 0;
+        if (e.key.load() == key) break;
+        if (e.key.compare_exchange_strong(empty, key)) {
+          e.per_sm.store(per_sm);
+          break;
+        }
+      }
+  }
   const int teams = rs.warps / rs.team;
   int64_t grid = (p.rows + teams - 1) / teams;
   const int64_t cap = static_cast<int64_t>(sm_count(device)) * per_sm;
