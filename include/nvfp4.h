@@ -150,6 +150,24 @@ nvfp4_status nvfp4_fused_roundtrip(const void* x, int64_t rows, int64_t cols,
                                    uint8_t* block_scales, float* scale, void* y, void* workspace,
                                    size_t workspace_bytes, nvfp4_stream_t stream);
 
+/* Bytes of device staging workspace nvfp4_fused_roundtrip_host needs for rows of `cols`
+ * elements (three chunk buffers of ~16 MB of input each); 0 for an invalid cols. */
+size_t nvfp4_roundtrip_host_workspace_bytes(int64_t cols);
+
+/* nvfp4_fused_roundtrip with the row scale for a matrix in HOST memory ("NVFP4 RL" Sec. 6: the
+ * same pipeline quantizes checkpoints online, from and to host memory).  x, codes, block_scales,
+ * row_scale and y are host pointers (page-locked memory lets the copies overlap; pageable memory
+ * works but serializes them); the layouts are those of the device calls.  Rows are streamed
+ * through `workspace` (device memory of at least nvfp4_roundtrip_host_workspace_bytes(cols)
+ * bytes, 256-byte aligned) in chunks on three internal streams, so host->device copies, kernels and
+ * device->host copies overlap.  Ordered after the work already queued on `stream`; `stream` is
+ * made to wait for all of it, so synchronize `stream` before reading the outputs.  Results are
+ * bit-identical to nvfp4_fused_roundtrip. */
+nvfp4_status nvfp4_fused_roundtrip_host(const void* x, int64_t rows, int64_t cols,
+                                        nvfp4_mode mode, uint8_t* codes, uint8_t* block_scales,
+                                        float* row_scale, void* y, void* workspace,
+                                        size_t workspace_bytes, nvfp4_stream_t stream);
+
 /* Reads (and, if clear != 0, resets to NVFP4_OK) the device status word of the current device.
  * Synchronizes the device.  *status_out receives NVFP4_OK or the first device-side error. */
 nvfp4_status nvfp4_get_device_status(int clear, nvfp4_status* status_out);

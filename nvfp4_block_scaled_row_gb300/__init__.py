@@ -70,6 +70,8 @@ def library():
         "nvfp4_quantize_tensor_noalloc": [P, I64, I64, I, P, P, P, P],
         "nvfp4_dequantize": [P, P, P, I, I64, I64, P, P],
         "nvfp4_fused_roundtrip": [P, I64, I64, I, I, P, P, P, P, P, SZ, P],
+        "nvfp4_roundtrip_host_workspace_bytes": [I64],
+        "nvfp4_fused_roundtrip_host": [P, I64, I64, I, P, P, P, P, P, SZ, P],
         "nvfp4_get_device_status": [I, P],
         "nvfp4_status_string": [I],
         "nvfp4_set_launch_config": [I, I, I],
@@ -81,6 +83,7 @@ def library():
         fn.argtypes = args
         fn.restype = I
     lib.nvfp4_tensor_workspace_bytes.restype = SZ
+    lib.nvfp4_roundtrip_host_workspace_bytes.restype = SZ
     lib.nvfp4_status_string.restype = ctypes.c_char_p
     _lib = lib
     return lib
@@ -269,6 +272,47 @@ def nvfp4_fused_roundtrip(x, kind="row", mode="four_over_six", codes=None, block
                                          ws_bytes, _stream(stream, dev))
     _check(st, "nvfp4_fused_roundtrip")
     return codes, block_scales, scale, y
+
+
+def nvfp4_roundtrip_host_workspace_bytes(cols):
+    return int(library().nvfp4_roundtrip_host_workspace_bytes(int(cols)))
+
+
+def _host(t, name, dtype, shape):
+    if t.is_cuda or t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host tensor {dtype} {tuple(shape)}")
+    return t
+
+
+def nvfp4_fused_roundtrip_host(x, mode="four_over_six", codes=None, block_scales=None,
+                               row_scale=None, y=None, workspace=None, stream=None, device=None):
+    """Per-token fused round trip of a HOST bf16 matrix, streamed through the GPU.  Outputs are
+    host tensors (allocated page-locked when not given).  Asynchronous on `stream`: synchronize it
+    before reading the outputs."""
+    if x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D bfloat16 host tensor")
+    rows, cols = x.shape
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+
+    def out(t, name, dtype, shape):
+        if t is None:
+            return torch.empty(shape, dtype=dtype, pin_memory=True)
+        return _host(t, name, dtype, shape)
+
+    codes = out(codes, "codes", torch.uint8, (rows, cols // 2))
+    block_scales = out(block_scales, "block_scales", torch.uint8, (rows, cols // 16))
+    row_scale = out(row_scale, "row_scale", torch.float32, (rows,))
+    y = out(y, "y", torch.bfloat16, (rows, cols))
+    need = nvfp4_roundtrip_host_workspace_bytes(cols)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = library().nvfp4_fused_roundtrip_host(_ptr(x), rows, cols, _MODES[mode], _ptr(codes),
+                                              _ptr(block_scales), _ptr(row_scale), _ptr(y),
+                                              _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(),
+                                              _stream(stream, dev))
+    _check(st, "nvfp4_fused_roundtrip_host")
+    return codes, block_scales, row_scale, y
 
 
 def nvfp4_get_device_status(clear=True):

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIBRARY = os.path.join(LIBDIR, "libnvfp4_gb300.so")
-SOURCES = ["nvfp4_quant.cu", "nvfp4_aux.cu", "nvfp4_capi.cu", "nvfp4_noalloc.cu"]
+SOURCES = ["nvfp4_quant.cu", "nvfp4_aux.cu", "nvfp4_capi.cu", "nvfp4_noalloc.cu", "nvfp4_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC]

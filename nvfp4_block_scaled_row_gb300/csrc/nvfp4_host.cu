@@ -1,0 +1,134 @@
+// nvfp4_host.cu -- quantize-and-dequantize of a matrix that lives in host memory, streamed through
+// the GPU in row chunks ("NVFP4 RL" blog, Sec. 6: the same pipeline serves online post-training
+// quantization of checkpoints, which starts and ends in host memory).
+//
+// Chunks rotate over three internal streams, each with its own third of the caller's device
+// staging workspace.  On each stream a chunk is copied in, quantized and dequantized by the fused
+// kernel, and its outputs are copied out; the other streams' chunks meanwhile use the other copy
+// direction and the SMs, so host->device copies, kernels and device->host copies overlap.  Events
+// order the internal streams after everything already queued on the caller's stream, and the
+// caller's stream after all of them, so the call behaves like any other asynchronous call on
+// `stream`.
+// Per-token results do not depend on chunking, so the outputs equal nvfp4_fused_roundtrip's.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "nvfp4.h"
+#include "nvfp4_internal.h"
+
+namespace {
+
+constexpr int64_t kChunkBytesTarget = 16ll << 20;  // ~16 MB of input per chunk
+constexpr int kStages = 3;                          // chunk buffers / internal streams
+
+struct ChunkLayout {
+  int64_t rows;   // rows per chunk
+  size_t x, codes, scales, sdec, y, total;  // byte offsets within one chunk buffer
+};
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+ChunkLayout layout_for(int64_t cols) {
+  ChunkLayout L;
+  L.rows = kChunkBytesTarget / (cols * 2);
+  if (L.rows < 1) L.rows = 1;
+  L.x = 0;
+  L.codes = align256(L.x + static_cast<size_t>(L.rows * cols * 2));
+  L.scales = align256(L.codes + static_cast<size_t>(L.rows * cols / 2));
+  L.sdec = align256(L.scales + static_cast<size_t>(L.rows * cols / 16));
+  L.y = align256(L.sdec + static_cast<size_t>(L.rows) * 4);
+  L.total = align256(L.y + static_cast<size_t>(L.rows * cols * 2));
+  return L;
+}
+
+}  // namespace
+
+extern "C" size_t nvfp4_roundtrip_host_workspace_bytes(int64_t cols) {
+  if (cols <= 0 || cols % nvfp4::kBlockElems != 0) return 0;
+  return kStages * layout_for(cols).total;
+}
+
+extern "C" nvfp4_status nvfp4_fused_roundtrip_host(const void* x, int64_t rows, int64_t cols,
+                                                   nvfp4_mode mode, uint8_t* codes,
+                                                   uint8_t* block_scales, float* row_scale,
+                                                   void* y, void* workspace,
+                                                   size_t workspace_bytes,
+                                                   nvfp4_stream_t stream) {
+  if ((mode != NVFP4_MODE_SIX && mode != NVFP4_MODE_FOUR_OVER_SIX) || rows < 0)
+    return NVFP4_ERR_INVALID_ARG;
+  if (cols <= 0 || cols % nvfp4::kBlockElems != 0 || !nvfp4::quantize_cols_supported(cols))
+    return NVFP4_ERR_SHAPE;
+  if (rows == 0) return NVFP4_OK;
+  if (x == nullptr || codes == nullptr || block_scales == nullptr || row_scale == nullptr ||
+      y == nullptr)
+    return NVFP4_ERR_INVALID_ARG;
+  const ChunkLayout L = layout_for(cols);
+  if (workspace == nullptr || workspace_bytes < kStages * L.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return NVFP4_ERR_WORKSPACE;
+
+  int* status = nullptr;
+  if (nvfp4::device_status_word(&status) != cudaSuccess) return NVFP4_ERR_CUDA;
+  cudaStream_t caller = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t s[kStages] = {};
+  cudaEvent_t start = nullptr, done[kStages] = {};
+  nvfp4_status result = NVFP4_OK;
+  auto check = [&](cudaError_t e) {
+    if (e != cudaSuccess && result == NVFP4_OK) result = NVFP4_ERR_CUDA;
+    return e == cudaSuccess;
+  };
+  if (!check(cudaEventCreateWithFlags(&start, cudaEventDisableTiming))) goto cleanup;
+  for (int i = 0; i < kStages; ++i)
+    if (!check(cudaStreamCreateWithFlags(&s[i], cudaStreamNonBlocking)) ||
+        !check(cudaEventCreateWithFlags(&done[i], cudaEventDisableTiming)))
+      goto cleanup;
+  if (!check(cudaEventRecord(start, caller))) goto cleanup;
+  for (int i = 0; i < kStages; ++i)
+    if (!check(cudaStreamWaitEvent(s[i], start, 0))) goto cleanup;
+
+  for (int64_t r0 = 0, c = 0; r0 < rows; r0 += L.rows, ++c) {
+    const int64_t n = (rows - r0 < L.rows) ? rows - r0 : L.rows;
+    const int h = static_cast<int>(c % kStages);
+    cudaStream_t st = s[h];
+    unsigned char* base = static_cast<unsigned char*>(workspace) + h * L.total;
+    const size_t xb = static_cast<size_t>(n * cols * 2);
+    const size_t cb = static_cast<size_t>(n * cols / 2);
+    const size_t sb = static_cast<size_t>(n * cols / 16);
+    if (!check(cudaMemcpyAsync(base + L.x, static_cast<const unsigned char*>(x) + r0 * cols * 2, xb,
+                               cudaMemcpyHostToDevice, st)))
+      break;
+    nvfp4::QuantParams p{};
+    p.x = reinterpret_cast<const uint16_t*>(base + L.x);
+    p.rows = n;
+    p.cols = static_cast<int32_t>(cols);
+    p.codes = base + L.codes;
+    p.scales = base + L.scales;
+    p.scale_out = reinterpret_cast<float*>(base + L.sdec);
+    p.y = reinterpret_cast<uint16_t*>(base + L.y);
+    p.status = status;
+    p.timeout_ns = 4000000000ull;
+    if (!check(nvfp4::launch_quantize(mode, false, true, p, st))) break;
+    if (!check(cudaMemcpyAsync(codes + r0 * cols / 2, base + L.codes, cb, cudaMemcpyDeviceToHost,
+                               st)) ||
+        !check(cudaMemcpyAsync(block_scales + r0 * cols / 16, base + L.scales, sb,
+                               cudaMemcpyDeviceToHost, st)) ||
+        !check(cudaMemcpyAsync(row_scale + r0, base + L.sdec, static_cast<size_t>(n) * 4,
+                               cudaMemcpyDeviceToHost, st)) ||
+        !check(cudaMemcpyAsync(static_cast<unsigned char*>(y) + r0 * cols * 2, base + L.y, xb,
+                               cudaMemcpyDeviceToHost, st)))
+      break;
+  }
+  // Whatever was queued, the caller's stream waits for all of it.
+  for (int i = 0; i < kStages; ++i)
+    if (check(cudaEventRecord(done[i], s[i]))) check(cudaStreamWaitEvent(caller, done[i], 0));
+
+cleanup:
+  // Destroying streams and events with work pending is allowed: they are released once it ends.
+  // (An early failure can leave the caller's stream without a wait: nothing was queued then.)
+  for (cudaStream_t st : s)
+    if (st != nullptr) cudaStreamDestroy(st);
+  if (start != nullptr) cudaEventDestroy(start);
+  for (cudaEvent_t e : done)
+    if (e != nullptr) cudaEventDestroy(e);
+  return result;
+}

@@ -139,3 +139,17 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(nv._build, "LIBRARY", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         nv.library()
+
+
+def test_host_roundtrip_validation(lib):
+    f = lib.nvfp4_fused_roundtrip_host
+    ws = nv.nvfp4_roundtrip_host_workspace_bytes(7168)
+    assert ws > 0 and nv.nvfp4_roundtrip_host_workspace_bytes(24) == 0
+    args = [P(1 << 20), 4, 7168, 1, P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20)]
+    assert f(*args, P(6 << 20), ws - 1, None) == WORKSPACE
+    assert f(*args, P((6 << 20) + 16), ws, None) == WORKSPACE
+    assert f(P(1 << 20), 4, 24, 1, P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20), P(6 << 20),
+             ws, None) == SHAPE
+    assert f(P(1 << 20), 0, 7168, 1, None, None, None, None, None, 0, None) == OK
+    assert f(None, 4, 7168, 1, P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20), P(6 << 20), ws,
+             None) == INVALID

@@ -297,3 +297,21 @@ def test_sharded_tensor_helper_on_one_rank():
     got = D.quantize_tensor_sharded(x)
     for a, b in zip(want, got):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+def test_host_streamed_roundtrip_matches_device_call():
+    """Host-resident input streamed in chunks (several chunks and a ragged last one) gives the
+    device call's outputs exactly, for both modes."""
+    x = synth.generate(2, device=DEV, rows=2500)["x"]
+    xh = x.cpu().pin_memory()
+    for mode in (F4, SIX):
+        want = nv.nvfp4_fused_roundtrip(x, "row", mode)
+        got = nv.nvfp4_fused_roundtrip_host(xh, mode)
+        torch.cuda.current_stream().synchronize()
+        for a, b in zip(want, got):
+            assert torch.equal(a.cpu().view(torch.uint8), b.view(torch.uint8))
+    # pageable host memory also works (serialized copies)
+    got = nv.nvfp4_fused_roundtrip_host(x[:300].cpu())
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(got[0], nv.nvfp4_fused_roundtrip(x[:300].contiguous())[0].cpu())
+    assert nv.nvfp4_get_device_status() == 0
