@@ -46,6 +46,8 @@ def algorithmic_bytes(rows, cols, op, scale_kind="row"):
         return quant + 2 * n
     if op == "dequantize":
         return n // 2 + n // 16 + scale_bytes + 2 * n
+    if op == "residual":  # x in; codes, scales and row scale for x and for its residual out
+        return 2 * n + 2 * (n // 2 + n // 16 + scale_bytes)
     raise ValueError(op)
 
 
@@ -266,6 +268,8 @@ def bench_op(nv, x, op, kind, mode, steps, warmup, world, device, offsets=None):
         codes, scales, scale = nv.nvfp4_quantize_tensor(x, mode)
         ws = torch.empty(nv.nvfp4_tensor_workspace_bytes(), dtype=torch.uint8, device=device)
         fn = lambda: nv.nvfp4_quantize_tensor(x, mode, codes, scales, scale, ws)
+    elif op == "residual":
+        fn = lambda: nv.nvfp4_quantize_residual(x, mode)
     else:  # dequantize
         codes, scales, scale = (nv.nvfp4_quantize_rowwise(x, mode) if kind == "row"
                                 else nv.nvfp4_quantize_tensor(x, mode))
@@ -406,7 +410,8 @@ def main():
                                     (1, "quantize", "tensor", "four_over_six"),
                                     (1, "quantize", "tensor", "six"),
                                     (1, "dequantize", "tensor", "four_over_six"),
-                                    (0, "quantize", "row", "four_over_six")):
+                                    (0, "quantize", "row", "four_over_six"),
+                                    (2, "residual", "row", "four_over_six")):
             ww = synth.workload(idx)
             d = synth.generate(idx, device=device)
             r = bench_op(nv, d["x"], op, kind, mode, max(5, args.steps // 2), 3, world, device,

@@ -87,6 +87,20 @@ nvfp4_status nvfp4_quantize_rowwise(const void* x, int64_t rows, int64_t cols,
                                     nvfp4_mode mode, uint8_t* codes, uint8_t* block_scales,
                                     float* row_scale, nvfp4_stream_t stream);
 
+/* Residual quantization in the manner of Rollout-ResQ ("HiFloat4 Format for End-To-End
+ * Reinforcement Learning Post-Training of Large Language Models", Rollout-ResQ section: the
+ * projection is computed as Q(X)Q(W) + Q(dX)Q(W) with dX = X - Q(X)), here with NVFP4 per-token
+ * 4/6 quantization for both terms:
+ *   (codes, block_scales, row_scale)             = Q(x), exactly as nvfp4_quantize_rowwise;
+ *   dX = bf16(fp32(x) - fp32(DQ(Q(x))))          (the difference is exact in FP32; one BF16 rounding);
+ *   (res_codes, res_block_scales, res_row_scale) = Q(dX) with dX's own per-token scale.
+ * One pass over x.  The 2:4 sparsification of the residual on that page is not applied.  Buffers,
+ * layouts and errors as nvfp4_quantize_rowwise; the two output sets must not overlap. */
+nvfp4_status nvfp4_quantize_residual(const void* x, int64_t rows, int64_t cols, nvfp4_mode mode,
+                                     uint8_t* codes, uint8_t* block_scales, float* row_scale,
+                                     uint8_t* res_codes, uint8_t* res_block_scales,
+                                     float* res_row_scale, nvfp4_stream_t stream);
+
 /* Bytes of device workspace the per-tensor calls need (a few KB; it holds partial maxima). */
 size_t nvfp4_tensor_workspace_bytes(void);
 

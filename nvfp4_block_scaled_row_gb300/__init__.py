@@ -17,7 +17,7 @@ from . import build as _build
 
 __all__ = [
     "Nvfp4Error", "MODE_SIX", "MODE_FOUR_OVER_SIX", "SCALE_ROW", "SCALE_TENSOR",
-    "nvfp4_quantize_rowwise", "nvfp4_quantize_tensor", "nvfp4_quantize_tensor_with_amax",
+    "nvfp4_quantize_rowwise", "nvfp4_quantize_residual", "nvfp4_quantize_tensor", "nvfp4_quantize_tensor_with_amax",
     "nvfp4_tensor_amax", "nvfp4_quantize_tensor_noalloc", "nvfp4_dequantize", "nvfp4_fused_roundtrip",
     "nvfp4_tensor_workspace_bytes", "nvfp4_get_device_status", "nvfp4_status_string",
     "nvfp4_set_launch_config", "nvfp4_selftest_wait_timeout", "nvfp4_abi_version", "library",
@@ -68,6 +68,7 @@ def library():
         "nvfp4_tensor_amax": [P, I64, P, P, SZ, P],
         "nvfp4_quantize_tensor_with_amax": [P, I64, I64, I, P, P, P, P, P],
         "nvfp4_quantize_tensor_noalloc": [P, I64, I64, I, P, P, P, P],
+        "nvfp4_quantize_residual": [P, I64, I64, I, P, P, P, P, P, P, P],
         "nvfp4_dequantize": [P, P, P, I, I64, I64, P, P],
         "nvfp4_fused_roundtrip": [P, I64, I64, I, I, P, P, P, P, P, SZ, P],
         "nvfp4_roundtrip_host_workspace_bytes": [I64],
@@ -143,6 +144,24 @@ def _workspace(workspace, device):
     elif not workspace.is_cuda or workspace.device != device:
         raise ValueError("workspace must be a CUDA tensor on the input's device")
     return workspace
+
+
+def nvfp4_quantize_residual(x, mode="four_over_six", stream=None):
+    """Q(x) and Q(dx), dx = bf16(x - DQ(Q(x))), both per-token 4/6, in one pass.  Returns
+    ((codes, block_scales, row_scale), (res_codes, res_block_scales, res_row_scale))."""
+    rows, cols = _input(x)
+    dev = x.device
+    outs = []
+    for _ in range(2):
+        outs.append((torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev),
+                     torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev),
+                     torch.empty((rows,), dtype=torch.float32, device=dev)))
+    (c, s, d), (rc, rs, rd) = outs
+    st = library().nvfp4_quantize_residual(_ptr(x), rows, cols, _MODES[mode], _ptr(c), _ptr(s),
+                                           _ptr(d), _ptr(rc), _ptr(rs), _ptr(rd),
+                                           _stream(stream, dev))
+    _check(st, "nvfp4_quantize_residual")
+    return outs[0], outs[1]
 
 
 def nvfp4_tensor_workspace_bytes():

@@ -177,6 +177,33 @@ nvfp4_status nvfp4_quantize_rowwise(const void* x, int64_t rows, int64_t cols,
   return from_cuda(launch_quantize(mode, false, false, p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+nvfp4_status nvfp4_quantize_residual(const void* x, int64_t rows, int64_t cols, nvfp4_mode mode,
+                                     uint8_t* codes, uint8_t* block_scales, float* row_scale,
+                                     uint8_t* res_codes, uint8_t* res_block_scales,
+                                     float* res_row_scale, nvfp4_stream_t stream) {
+  bool noop = false;
+  nvfp4_status st = check_quantize(x, rows, cols, mode, codes, block_scales, row_scale, false,
+                                   nullptr, false, &noop);
+  if (st != NVFP4_OK || noop) return st;
+  st = check_quantize(x, rows, cols, mode, res_codes, res_block_scales, res_row_scale, false,
+                      nullptr, false, &noop);
+  if (st != NVFP4_OK) return st;
+  const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols);
+  const void* a[3] = {codes, block_scales, row_scale};
+  const size_t an[3] = {n / 2, n / 16, 4 * static_cast<size_t>(rows)};
+  const void* b[3] = {res_codes, res_block_scales, res_row_scale};
+  for (int i = 0; i < 3; ++i)
+    for (int j = 0; j < 3; ++j)
+      if (overlap(a[i], an[i], b[j], an[j])) return NVFP4_ERR_INVALID_ARG;
+  int* status = nullptr;
+  if (status_ptr(&status) != cudaSuccess) return NVFP4_ERR_CUDA;
+  QuantParams p = base_params(x, rows, cols, codes, block_scales, row_scale, nullptr, status);
+  p.res_codes = res_codes;
+  p.res_scales = res_block_scales;
+  p.res_scale_out = res_row_scale;
+  return from_cuda(launch_quantize_residual(mode, p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t nvfp4_tensor_workspace_bytes(void) {
   return static_cast<size_t>(kAmaxMaxPartials) * sizeof(float);
 }

@@ -23,7 +23,7 @@ constexpr int kAmaxMaxPartials = 1024;   // per-tensor amax: partial maxima in t
 
 // Shared-memory header of the quantize kernel, then the ring (128-byte aligned).
 constexpr int kTableBytes = 256 * 8;                          // one ScaleEntry per E4M3 byte
-constexpr int kXchBytes = 2 * kMaxWarpsPerCta * 4;            // row-amax partials, 2 parities
+constexpr int kXchBytes = 4 * kMaxWarpsPerCta * 4;            // row-amax partials: 2 parities x 2 tensors
 constexpr int kAbortBytes = kMaxWarpsPerCta * 4;              // per-team abort flags
 constexpr int kBarrierBytes = kMaxWarpsPerCta * kMaxStages * 8;
 constexpr int kHeaderBytes =
@@ -52,6 +52,9 @@ struct QuantParams {
   uint8_t* scales;          // [rows][cols/16]
   float* scale_out;         // S_dec: [rows] (row scale) or [1] (tensor scale)
   uint16_t* y;              // BF16 bits [rows][cols], fused round trip only
+  uint8_t* res_codes;       // residual quantization outputs (residual kernels only)
+  uint8_t* res_scales;
+  float* res_scale_out;
   const float* amax_src;    // tensor scale: n_amax partial maxima (or one amax)
   int32_t n_amax;
   const int32_t* offsets;   // optional group offsets [num_groups + 1]
@@ -321,6 +324,12 @@ __device__ __forceinline__ ScaleEntry make_scale_entry(uint32_t byte) {
   e.inv = (s == 0.0f || !(s == s)) ? 0.0f : __frcp_rn(s);
   e.neg_s_h2 = h2 ^ 0x80008000u;
   return e;
+}
+
+// Orders this thread's earlier generic-proxy shared-memory writes before later async-proxy
+// (bulk copy) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Named barrier over `threads` threads (a multiple of 32) of the CTA.

@@ -25,6 +25,10 @@ int sm_count(int device);
 cudaError_t launch_quantize(int mode, bool tensor_scale, bool fused, QuantParams p,
                             cudaStream_t stream);
 
+// Row-scale quantization of x and of its BF16 residual x - DQ(Q(x)) in one pass over x
+// (p.res_codes, p.res_scales, p.res_scale_out receive the residual's outputs).
+cudaError_t launch_quantize_residual(int mode, QuantParams p, cudaStream_t stream);
+
 // Whether the quantize kernels can stage a row of `cols` BF16 values.
 bool quantize_cols_supported(int64_t cols);
 

@@ -103,6 +103,81 @@ __device__ __forceinline__ Candidate encode_candidate(const f32x2 (&z)[8], const
   return c;
 }
 
+// Encodes one 16-element block with block amax m: both candidates (scale-to-6 only in mode six),
+// the 4/6 choice, then stores the 8 code bytes and the E4M3 scale byte.  Half A holds elements
+// 8*h0 .. 8*h0+7 of the block, half B the other eight.  With kWantY, `out` receives the block's
+// dequantized BF16 pairs (A's four words, then B's) = bf16(fp32(q*s) * S_dec).
+template <int kMode, bool kWantY>
+__device__ __forceinline__ void encode_block(const uint4 A, const uint4 B, float m,
+                                             const RowFactors& f, const ScaleEntry* tab, int h0,
+                                             uint8_t* codes_blk, uint8_t* scale_ptr,
+                                             uint32_t (&out)[8]) {
+  const f32x2 senc2 = pack2(f.S_enc, f.S_enc);
+  const uint16_t one_bf16 = 0x3F80;
+  const float neg_zero = -0.0f;
+  const float u6 = __fmul_rn(m, f.c6);
+  const float u4 = (kMode == kModeFourOverSix) ? __fmul_rn(m, f.c4) : 0.0f;
+  const uint32_t sb = e4m3x2_from_f32(u4, u6);
+  const uint32_t b6 = sb & 0xFFu, b4 = sb >> 8;
+
+  f32x2 z[8];
+  z[0] = mul2(bf16x2_to_f32x2_fma(A.x, one_bf16, neg_zero), senc2);
+  z[1] = mul2(bf16x2_to_f32x2_fma(A.y, one_bf16, neg_zero), senc2);
+  z[2] = mul2(bf16x2_to_f32x2_fma(A.z, one_bf16, neg_zero), senc2);
+  z[3] = mul2(bf16x2_to_f32x2_fma(A.w, one_bf16, neg_zero), senc2);
+  z[4] = mul2(bf16x2_to_f32x2_fma(B.x, one_bf16, neg_zero), senc2);
+  z[5] = mul2(bf16x2_to_f32x2_fma(B.y, one_bf16, neg_zero), senc2);
+  z[6] = mul2(bf16x2_to_f32x2_fma(B.z, one_bf16, neg_zero), senc2);
+  z[7] = mul2(bf16x2_to_f32x2_fma(B.w, one_bf16, neg_zero), senc2);
+
+  const ScaleEntry e6 = tab[b6];
+  const Candidate c6 = encode_candidate(z, e6);
+  bool pick4 = false;
+  Candidate c4{};
+  ScaleEntry e4{};
+  if (kMode == kModeFourOverSix) {
+    e4 = tab[b4];
+    c4 = encode_candidate(z, e4);
+    pick4 = c4.err < c6.err;  // ties go to 6
+  }
+  uint32_t* cw = reinterpret_cast<uint32_t*>(codes_blk);
+  cw[h0] = pick4 ? c4.cw[0] : c6.cw[0];
+  cw[1 - h0] = pick4 ? c4.cw[1] : c6.cw[1];
+  *scale_ptr = static_cast<uint8_t>(pick4 ? b4 : b6);
+
+  if (kWantY) {
+    const uint32_t s_h2 = (pick4 ? e4.neg_s_h2 : e6.neg_s_h2) ^ 0x80008000u;
+    const f32x2 sdec2 = pack2(f.S_dec, f.S_dec);
+    const f32x2 nzero = pack2(-0.0f, -0.0f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t r = pick4 ? c4.r[j] : c6.r[j];
+      const f32x2 qs = fma_f16x2_f32x2(r, s_h2, nzero);  // q*s, exact
+      out[j] = bf16x2_from_f32x2(mul2(qs, sdec2));
+    }
+  }
+}
+
+// BF16 residual pair bf16(fp32(x) - fp32(y)) of two BF16 pairs (the difference is exact in FP32).
+__device__ __forceinline__ uint32_t bf16x2_residual(uint32_t xw, uint32_t yw) {
+  const uint16_t one_bf16 = 0x3F80;
+  const float neg_zero = -0.0f;
+  const f32x2 xf = bf16x2_to_f32x2_fma(xw, one_bf16, neg_zero);
+  const f32x2 yf = bf16x2_to_f32x2_fma(yw, one_bf16, neg_zero);
+  return bf16x2_from_f32x2(fma2(yf, pack2(-1.0f, -1.0f), xf));
+}
+
+// Both halves of the result hold the largest |value| of a BF16 pair word (sign bits arbitrary).
+__device__ __forceinline__ float abs_max_word(uint32_t mx) {
+  const uint32_t mm = max_abs_bf16x2(mx, __byte_perm(mx, 0, 0x1032));
+  return fabsf(__uint_as_float(mm << 16));
+}
+
+__device__ __forceinline__ uint32_t block_max_word(const uint4 A, const uint4 B) {
+  return max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(A.x, A.y), max_abs_bf16x2(A.z, A.w)),
+                        max_abs_bf16x2(max_abs_bf16x2(B.x, B.y), max_abs_bf16x2(B.z, B.w)));
+}
+
 // Shared-memory layout: [table | amax exchange | abort flags | barriers] (kHeaderBytes), then the
 // ring: warp w owns `stages` slots of `slot_bytes`.
 //
@@ -111,7 +186,7 @@ __device__ __forceinline__ Candidate encode_candidate(const f32x2 (&z)[8], const
 // gt, gt + NT, gt + 2NT, ... (gt = global team index, NT = number of teams).  With more than one
 // warp per team the row amax is combined through shared memory behind a named barrier; if any
 // member's copy times out, all members leave together after that barrier.
-template <int kMode, bool kTensor, bool kFused>
+template <int kMode, bool kTensor, bool kFused, bool kResidual>
 __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const QuantParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   ScaleEntry* tab = reinterpret_cast<ScaleEntry*>(smem);
@@ -200,7 +275,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
                                   p.timeout_ns);
       return;
     }
-    const unsigned char* xs = my_ring + static_cast<size_t>(slot) * p.slot_bytes;
+    unsigned char* xs = my_ring + static_cast<size_t>(slot) * p.slot_bytes;
 
     // Pass 1 (row scale): block maxima (kept in registers for pass 2) and the row amax.
     uint32_t bmax[kMaxBlocksPerLane];
@@ -214,9 +289,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
           const unsigned char* blk = xs + (b - b0) * 32;
           const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
           const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
-          bmax[j] = max_abs_bf16x2(
-              max_abs_bf16x2(max_abs_bf16x2(A.x, A.y), max_abs_bf16x2(A.z, A.w)),
-              max_abs_bf16x2(max_abs_bf16x2(B.x, B.y), max_abs_bf16x2(B.z, B.w)));
+          bmax[j] = block_max_word(A, B);
           m2 = max_abs_bf16x2(m2, bmax[j]);
         }
       }
@@ -244,76 +317,68 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
       if (lane == 0 && tw == 0) p.scale_out[row] = f.S_dec;
     }
 
-    // Pass 2: encode this warp's blocks.
-    const f32x2 senc2 = pack2(f.S_enc, f.S_enc);
-    const uint16_t one_bf16 = 0x3F80;
-    const float neg_zero = -0.0f;
+    // Pass 2: encode this warp's blocks (residual kernels also turn each block into its BF16
+    // residual x - DQ(Q(x)) in place, with the residual's block maxima kept for pass 3).
     uint8_t* codes_row = p.codes + row * (cols / 2);
     uint8_t* scales_row = p.scales + row * nblk;
+    uint32_t rmax[kMaxBlocksPerLane];
+    uint32_t rm2 = 0;
 #pragma unroll
     for (int j = 0; j < kMaxBlocksPerLane; ++j) {
       const int b = b0 + lane + 32 * j;
       if (b >= b1) break;
-      const unsigned char* blk = xs + (b - b0) * 32;
+      unsigned char* blk = xs + (b - b0) * 32;
       const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
       const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
-      uint32_t mx;
-      if (kTensor) {
-        mx = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(A.x, A.y), max_abs_bf16x2(A.z, A.w)),
-                            max_abs_bf16x2(max_abs_bf16x2(B.x, B.y), max_abs_bf16x2(B.z, B.w)));
-      } else {
-        mx = bmax[j];
-      }
-      // Both halves of `mm` hold the block's largest |x| (sign bits arbitrary; fabsf drops them).
-      const uint32_t mm = max_abs_bf16x2(mx, __byte_perm(mx, 0, 0x1032));
-      const float m = fabsf(__uint_as_float(mm << 16));
-      const float u6 = __fmul_rn(m, f.c6);
-      const float u4 = (kMode == kModeFourOverSix) ? __fmul_rn(m, f.c4) : 0.0f;
-      const uint32_t sb = e4m3x2_from_f32(u4, u6);
-      const uint32_t b6 = sb & 0xFFu, b4 = sb >> 8;
-
-      f32x2 z[8];
-      z[0] = mul2(bf16x2_to_f32x2_fma(A.x, one_bf16, neg_zero), senc2);
-      z[1] = mul2(bf16x2_to_f32x2_fma(A.y, one_bf16, neg_zero), senc2);
-      z[2] = mul2(bf16x2_to_f32x2_fma(A.z, one_bf16, neg_zero), senc2);
-      z[3] = mul2(bf16x2_to_f32x2_fma(A.w, one_bf16, neg_zero), senc2);
-      z[4] = mul2(bf16x2_to_f32x2_fma(B.x, one_bf16, neg_zero), senc2);
-      z[5] = mul2(bf16x2_to_f32x2_fma(B.y, one_bf16, neg_zero), senc2);
-      z[6] = mul2(bf16x2_to_f32x2_fma(B.z, one_bf16, neg_zero), senc2);
-      z[7] = mul2(bf16x2_to_f32x2_fma(B.w, one_bf16, neg_zero), senc2);
-
-      const ScaleEntry e6 = tab[b6];
-      const Candidate c6 = encode_candidate(z, e6);
-      bool pick4 = false;
-      Candidate c4{};
-      ScaleEntry e4{};
-      if (kMode == kModeFourOverSix) {
-        e4 = tab[b4];
-        c4 = encode_candidate(z, e4);
-        pick4 = c4.err < c6.err;  // ties go to 6
-      }
-      const uint32_t wA = pick4 ? c4.cw[0] : c6.cw[0];
-      const uint32_t wB = pick4 ? c4.cw[1] : c6.cw[1];
-      uint32_t* cw = reinterpret_cast<uint32_t*>(codes_row + b * 8);
-      cw[h0] = wA;  // half A holds elements 8*h0 .. 8*h0+7 of the block
-      cw[1 - h0] = wB;
-      scales_row[b] = static_cast<uint8_t>(pick4 ? b4 : b6);
-
+      const float m = abs_max_word(kTensor ? block_max_word(A, B) : bmax[j]);
+      uint32_t out[8];
+      encode_block<kMode, kFused || kResidual>(A, B, m, f, tab, h0, codes_row + b * 8,
+                                               scales_row + b, out);
       if (kFused) {
-        const uint32_t s_h2 = (pick4 ? e4.neg_s_h2 : e6.neg_s_h2) ^ 0x80008000u;
-        const f32x2 sdec2 = pack2(f.S_dec, f.S_dec);
-        const f32x2 nzero = pack2(-0.0f, -0.0f);
-        uint32_t out[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t r = pick4 ? c4.r[j] : c6.r[j];
-          const f32x2 qs = fma_f16x2_f32x2(r, s_h2, nzero);  // q*s, exact
-          out[j] = bf16x2_from_f32x2(mul2(qs, sdec2));
-        }
         uint16_t* y_blk = p.y + row * cols + b * kBlockElems;
         *reinterpret_cast<uint4*>(y_blk + h0 * 8) = make_uint4(out[0], out[1], out[2], out[3]);
         *reinterpret_cast<uint4*>(y_blk + (1 - h0) * 8) = make_uint4(out[4], out[5], out[6], out[7]);
       }
+      if (kResidual) {
+        const uint4 RA = make_uint4(bf16x2_residual(A.x, out[0]), bf16x2_residual(A.y, out[1]),
+                                    bf16x2_residual(A.z, out[2]), bf16x2_residual(A.w, out[3]));
+        const uint4 RB = make_uint4(bf16x2_residual(B.x, out[4]), bf16x2_residual(B.y, out[5]),
+                                    bf16x2_residual(B.z, out[6]), bf16x2_residual(B.w, out[7]));
+        *reinterpret_cast<uint4*>(blk + h0 * 16) = RA;
+        *reinterpret_cast<uint4*>(blk + (1 - h0) * 16) = RB;
+        rmax[j] = block_max_word(RA, RB);
+        rm2 = max_abs_bf16x2(rm2, rmax[j]);
+      }
+    }
+
+    if (kResidual) {
+      // Pass 3: the residual's own per-token scale, then its blocks.
+      float a = abs_max_of_pair(rm2);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+      if (TW > 1) {
+        float* part = xch + (2 + (k & 1)) * kMaxWarpsPerCta;
+        if (lane == 0) part[warp] = a;
+        named_barrier(1 + team, TW * 32);
+        a = 0.0f;
+        for (int j = 0; j < TW; ++j) a = fmaxf(a, part[team * TW + j]);
+      }
+      const RowFactors g = row_factors_warp<kMode>(a, lane);
+      if (lane == 0 && tw == 0) p.res_scale_out[row] = g.S_dec;
+      uint8_t* rcodes_row = p.res_codes + row * (cols / 2);
+      uint8_t* rscales_row = p.res_scales + row * nblk;
+#pragma unroll
+      for (int j = 0; j < kMaxBlocksPerLane; ++j) {
+        const int b = b0 + lane + 32 * j;
+        if (b >= b1) break;
+        const unsigned char* blk = xs + (b - b0) * 32;
+        const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
+        const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
+        uint32_t unused[8];
+        encode_block<kMode, false>(A, B, abs_max_word(rmax[j]), g, tab, h0, rcodes_row + b * 8,
+                                   rscales_row + b, unused);
+      }
+      fence_proxy_async_smem();  // the residual writes above precede the slot's next bulk copy
     }
 
     // Slot consumed: refill it with this warp's part of the row `stages` steps ahead.
@@ -382,12 +447,12 @@ struct LaunchCache {
   } entries[kDevices][kShapes];
 };
 
-template <int kMode, bool kTensor, bool kFused>
+template <int kMode, bool kTensor, bool kFused, bool kResidual>
 cudaError_t launch_impl(QuantParams p, cudaStream_t stream) {
   static LaunchCache cache;
   RingShape rs;
   if (!choose_ring(p.cols, &rs)) return cudaErrorInvalidValue;
-  auto kern = quantize_kernel<kMode, kTensor, kFused>;
+  auto kern = quantize_kernel<kMode, kTensor, kFused, kResidual>;
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
@@ -447,16 +512,21 @@ cudaError_t launch_quantize(int mode, bool tensor_scale, bool fused, QuantParams
                             cudaStream_t stream) {
   if (mode == kModeFourOverSix) {
     if (tensor_scale)
-      return fused ? launch_impl<kModeFourOverSix, true, true>(p, stream)
-                   : launch_impl<kModeFourOverSix, true, false>(p, stream);
-    return fused ? launch_impl<kModeFourOverSix, false, true>(p, stream)
-                 : launch_impl<kModeFourOverSix, false, false>(p, stream);
+      return fused ? launch_impl<kModeFourOverSix, true, true, false>(p, stream)
+                   : launch_impl<kModeFourOverSix, true, false, false>(p, stream);
+    return fused ? launch_impl<kModeFourOverSix, false, true, false>(p, stream)
+                 : launch_impl<kModeFourOverSix, false, false, false>(p, stream);
   }
   if (tensor_scale)
-    return fused ? launch_impl<kModeSix, true, true>(p, stream)
-                 : launch_impl<kModeSix, true, false>(p, stream);
-  return fused ? launch_impl<kModeSix, false, true>(p, stream)
-               : launch_impl<kModeSix, false, false>(p, stream);
+    return fused ? launch_impl<kModeSix, true, true, false>(p, stream)
+                 : launch_impl<kModeSix, true, false, false>(p, stream);
+  return fused ? launch_impl<kModeSix, false, true, false>(p, stream)
+               : launch_impl<kModeSix, false, false, false>(p, stream);
+}
+
+cudaError_t launch_quantize_residual(int mode, QuantParams p, cudaStream_t stream) {
+  return mode == kModeFourOverSix ? launch_impl<kModeFourOverSix, false, false, true>(p, stream)
+                                  : launch_impl<kModeSix, false, false, true>(p, stream);
 }
 
 }  // namespace nvfp4

@@ -49,6 +49,8 @@ def _load():
     lib.oracle_quantize.argtypes = [P, I64, I64, I, I, P, P, P, P, P]
     lib.oracle_quantize_given_amax.restype = I
     lib.oracle_quantize_given_amax.argtypes = [P, I64, I64, I, ctypes.c_float, P, P, P]
+    lib.oracle_quantize_residual.restype = I
+    lib.oracle_quantize_residual.argtypes = [P, I64, I64, I, P, P, P, P, P, P]
     lib.oracle_dequantize.restype = I
     lib.oracle_dequantize.argtypes = [P, P, P, I, I64, I64, P]
     for name in ("oracle_e2m1_encode_array", "oracle_e4m3_encode_array",
@@ -153,6 +155,25 @@ def quantize_given_amax(x_u16, amax_value, mode=MODE_FOUR_OVER_SIX):
     if rc:
         raise ValueError("oracle_quantize_given_amax rejected its arguments")
     return {"codes": codes, "scales": scales, "scale": scale}
+
+
+def quantize_residual(x_u16, mode=MODE_FOUR_OVER_SIX):
+    """Q(x) and Q(dx), dx = bf16(x - DQ(Q(x))), both per-token: returns (main, residual) dicts
+    shaped like quantize()'s."""
+    x = _u16(x_u16)
+    rows, cols = x.shape
+    outs = []
+    for _ in range(2):
+        outs.append({"codes": np.zeros((rows, cols // 2), np.uint8),
+                     "scales": np.zeros((rows, cols // BLOCK), np.uint8),
+                     "scale": np.zeros(rows, np.float32)})
+    a, b = outs
+    rc = _load().oracle_quantize_residual(_ptr(x), rows, cols, int(mode), _ptr(a["codes"]),
+                                          _ptr(a["scales"]), _ptr(a["scale"]), _ptr(b["codes"]),
+                                          _ptr(b["scales"]), _ptr(b["scale"]))
+    if rc:
+        raise ValueError("oracle_quantize_residual rejected its arguments")
+    return a, b
 
 
 def dequantize(codes, scales, scale, scale_kind=SCALE_ROW):

@@ -45,6 +45,7 @@
 #include <float.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORACLE_MODE_SIX 0
@@ -306,6 +307,38 @@ int oracle_dequantize(const uint8_t* codes, const uint8_t* scales, const float* 
       y[r * cols + k] = oracle_bf16_encode(qs * S_dec);
     }
   }
+  return 0;
+}
+
+/* Residual quantization after Rollout-ResQ ("HiFloat4 Format for End-To-End Reinforcement
+ * Learning Post-Training of Large Language Models", Rollout-ResQ section: dX = X - Q(X), then
+ * Q(X) and Q(dX) are both used), with per-token NVFP4 4/6 for both terms.  Per row: Q(x);
+ * y = DQ(Q(x)); the residual dx = bf16(fp32(x) - fp32(y)); Q(dx) with dx's own row scale. */
+int oracle_quantize_residual(const uint16_t* x, int64_t rows, int64_t cols, int mode,
+                             uint8_t* codes, uint8_t* scales, float* scale_out, uint8_t* res_codes,
+                             uint8_t* res_scales, float* res_scale_out) {
+  if (check_shape(rows, cols, mode)) return 1;
+  uint16_t* y = (uint16_t*)malloc((size_t)cols * sizeof(uint16_t));
+  uint16_t* dx = (uint16_t*)malloc((size_t)cols * sizeof(uint16_t));
+  if (!y || !dx) {
+    free(y);
+    free(dx);
+    return 1;
+  }
+  int64_t nb = cols / ORACLE_BLOCK;
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint16_t* xr = x + r * cols;
+    quantize_rows(xr, 1, cols, mode, 1, 0.0f, codes + r * (cols / 2), scales + r * nb,
+                  scale_out + r, 0, 0);
+    oracle_dequantize(codes + r * (cols / 2), scales + r * nb, scale_out + r, ORACLE_SCALE_ROW, 1,
+                      cols, y);
+    for (int64_t k = 0; k < cols; ++k)
+      dx[k] = oracle_bf16_encode(oracle_bf16_to_f32(xr[k]) - oracle_bf16_to_f32(y[k]));
+    quantize_rows(dx, 1, cols, mode, 1, 0.0f, res_codes + r * (cols / 2), res_scales + r * nb,
+                  res_scale_out + r, 0, 0);
+  }
+  free(y);
+  free(dx);
   return 0;
 }
 

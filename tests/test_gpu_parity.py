@@ -315,3 +315,35 @@ def test_host_streamed_roundtrip_matches_device_call():
     torch.cuda.current_stream().synchronize()
     assert torch.equal(got[0], nv.nvfp4_fused_roundtrip(x[:300].contiguous())[0].cpu())
     assert nv.nvfp4_get_device_status() == 0
+
+
+def check_residual(x, mode=F4, rows_idx=None):
+    xs = x if rows_idx is None else x[torch.as_tensor(rows_idx, device=x.device)]
+    want_m, want_r = oracle.quantize_residual(synth.as_u16(xs), OMODE[mode])
+    (c, s, d), (rc, rs, rd) = nv.nvfp4_quantize_residual(x, mode)
+    if rows_idx is not None:
+        idx = torch.as_tensor(rows_idx, device=x.device)
+        c, s, d, rc, rs, rd = (t[idx] for t in (c, s, d, rc, rs, rd))
+    for got, want, what in ((c, want_m["codes"], "codes"), (s, want_m["scales"], "scales"),
+                            (d, want_m["scale"], "row scale"), (rc, want_r["codes"], "res codes"),
+                            (rs, want_r["scales"], "res scales"),
+                            (rd, want_r["scale"], "res row scale")):
+        _assert_equal(_np(got), want, what)
+    assert nv.nvfp4_get_device_status() == 0
+
+
+@pytest.mark.parametrize("index,rows", [(0, None), (2, 300), (3, 640), (4, 500)])
+def test_residual_workloads(index, rows):
+    x = synth.generate(index, device=DEV, rows=rows)["x"]
+    check_residual(x)
+    check_residual(x, SIX)
+
+
+@pytest.mark.parametrize("cols", [16, 48, 2064, 7168, 7184, 32768])
+def test_residual_edge_values(cols):
+    check_residual(_edge_matrix(3 if cols >= 16384 else 21, cols, seed=cols + 1))
+
+
+def test_residual_full_size_sampled():
+    x = synth.generate(2, device=DEV)["x"]
+    check_residual(x, F4, _sample_rows(x.shape[0], n=32, seed=7))
