@@ -48,6 +48,8 @@ def algorithmic_bytes(rows, cols, op, scale_kind="row"):
         return n // 2 + n // 16 + scale_bytes + 2 * n
     if op == "residual":  # x in; codes, scales and row scale for x and for its residual out
         return 2 * n + 2 * (n // 2 + n // 16 + scale_bytes)
+    if op == "guided":  # x, rollout amax, codes and scales in; codes out
+        return 2 * n + n // 2 + n // 16 + scale_bytes + n // 2
     raise ValueError(op)
 
 
@@ -270,6 +272,11 @@ def bench_op(nv, x, op, kind, mode, steps, warmup, world, device, offsets=None):
         fn = lambda: nv.nvfp4_quantize_tensor(x, mode, codes, scales, scale, ws)
     elif op == "residual":
         fn = lambda: nv.nvfp4_quantize_residual(x, mode)
+    elif op == "guided":
+        amax = nv.nvfp4_row_amax(x)
+        rc, rs, _ = nv.nvfp4_quantize_rowwise(x, mode)
+        out = torch.empty_like(rc)
+        fn = lambda: nv.nvfp4_quantize_guided(x, amax, rc, rs, mode, out)
     else:  # dequantize
         codes, scales, scale = (nv.nvfp4_quantize_rowwise(x, mode) if kind == "row"
                                 else nv.nvfp4_quantize_tensor(x, mode))
@@ -411,7 +418,8 @@ def main():
                                     (1, "quantize", "tensor", "six"),
                                     (1, "dequantize", "tensor", "four_over_six"),
                                     (0, "quantize", "row", "four_over_six"),
-                                    (2, "residual", "row", "four_over_six")):
+                                    (2, "residual", "row", "four_over_six"),
+                                    (2, "guided", "row", "four_over_six")):
             ww = synth.workload(idx)
             d = synth.generate(idx, device=device)
             r = bench_op(nv, d["x"], op, kind, mode, max(5, args.steps // 2), 3, world, device,

@@ -101,6 +101,26 @@ nvfp4_status nvfp4_quantize_residual(const void* x, int64_t rows, int64_t cols, 
                                      uint8_t* res_codes, uint8_t* res_block_scales,
                                      float* res_row_scale, nvfp4_stream_t stream);
 
+/* Per-token amax: row_amax[r] = max_k |x[r][k]| (device float [rows]).  What a rollout records
+ * so that a later nvfp4_quantize_guided reproduces its scales. */
+nvfp4_status nvfp4_row_amax(const void* x, int64_t rows, int64_t cols, float* row_amax,
+                            nvfp4_stream_t stream);
+
+/* Rollout-guided rounding ("TRACE FP4 RL -- Rollout-guided FP4 rounding": between the two
+ * neighbouring codewords of its own value the training engine picks the one closer to the
+ * codeword the rollout recorded, under the rollout-side scale).  Inputs: the trainer's x, the
+ * rollout's per-token amax (row_amax, device float [rows]), its codes and its E4M3 block scales
+ * (layouts as nvfp4_quantize_rowwise).  Each element's scaled value t is formed as the quantizer
+ * forms it from that amax and block scale; the output code is whichever of t's two neighbouring
+ * E2M1 codewords (one if t is on the grid or beyond +-6) is closer to the rollout's codeword, with
+ * the sign of t kept on zero.  The block scales and row scales stay the rollout's.  When x equals
+ * the rollout's input the output equals the rollout's codes.  codes: device uint8 [rows][cols/2].
+ * Any cols that is a positive multiple of 16. */
+nvfp4_status nvfp4_quantize_guided(const void* x, int64_t rows, int64_t cols, nvfp4_mode mode,
+                                   const float* row_amax, const uint8_t* ref_codes,
+                                   const uint8_t* ref_block_scales, uint8_t* codes,
+                                   nvfp4_stream_t stream);
+
 /* Bytes of device workspace the per-tensor calls need (a few KB; it holds partial maxima). */
 size_t nvfp4_tensor_workspace_bytes(void);
 

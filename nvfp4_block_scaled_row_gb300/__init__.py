@@ -17,7 +17,7 @@ from . import build as _build
 
 __all__ = [
     "Nvfp4Error", "MODE_SIX", "MODE_FOUR_OVER_SIX", "SCALE_ROW", "SCALE_TENSOR",
-    "nvfp4_quantize_rowwise", "nvfp4_quantize_residual", "nvfp4_quantize_tensor", "nvfp4_quantize_tensor_with_amax",
+    "nvfp4_quantize_rowwise", "nvfp4_quantize_residual", "nvfp4_row_amax", "nvfp4_quantize_guided", "nvfp4_quantize_tensor", "nvfp4_quantize_tensor_with_amax",
     "nvfp4_tensor_amax", "nvfp4_quantize_tensor_noalloc", "nvfp4_dequantize", "nvfp4_fused_roundtrip",
     "nvfp4_tensor_workspace_bytes", "nvfp4_get_device_status", "nvfp4_status_string",
     "nvfp4_set_launch_config", "nvfp4_selftest_wait_timeout", "nvfp4_abi_version", "library",
@@ -69,6 +69,8 @@ def library():
         "nvfp4_quantize_tensor_with_amax": [P, I64, I64, I, P, P, P, P, P],
         "nvfp4_quantize_tensor_noalloc": [P, I64, I64, I, P, P, P, P],
         "nvfp4_quantize_residual": [P, I64, I64, I, P, P, P, P, P, P, P],
+        "nvfp4_row_amax": [P, I64, I64, P, P],
+        "nvfp4_quantize_guided": [P, I64, I64, I, P, P, P, P, P],
         "nvfp4_dequantize": [P, P, P, I, I64, I64, P, P],
         "nvfp4_fused_roundtrip": [P, I64, I64, I, I, P, P, P, P, P, SZ, P],
         "nvfp4_roundtrip_host_workspace_bytes": [I64],
@@ -162,6 +164,31 @@ def nvfp4_quantize_residual(x, mode="four_over_six", stream=None):
                                            _stream(stream, dev))
     _check(st, "nvfp4_quantize_residual")
     return outs[0], outs[1]
+
+
+def nvfp4_row_amax(x, row_amax=None, stream=None):
+    """Per-token amax, float32 [rows]."""
+    rows, cols = _input(x)
+    row_amax = _out(row_amax, "row_amax", torch.float32, (rows,), x.device)
+    _check(library().nvfp4_row_amax(_ptr(x), rows, cols, _ptr(row_amax), _stream(stream, x.device)),
+           "nvfp4_row_amax")
+    return row_amax
+
+
+def nvfp4_quantize_guided(x, row_amax, ref_codes, ref_block_scales, mode="four_over_six",
+                          codes=None, stream=None):
+    """TRACE-guided codes for x under a rollout's per-token amax, codes and block scales."""
+    rows, cols = _input(x)
+    dev = x.device
+    _need(row_amax, "row_amax", torch.float32, (rows,), dev)
+    _need(ref_codes, "ref_codes", torch.uint8, (rows, cols // 2), dev)
+    _need(ref_block_scales, "ref_block_scales", torch.uint8, (rows, cols // 16), dev)
+    codes = _out(codes, "codes", torch.uint8, (rows, cols // 2), dev)
+    st = library().nvfp4_quantize_guided(_ptr(x), rows, cols, _MODES[mode], _ptr(row_amax),
+                                         _ptr(ref_codes), _ptr(ref_block_scales), _ptr(codes),
+                                         _stream(stream, dev))
+    _check(st, "nvfp4_quantize_guided")
+    return codes
 
 
 def nvfp4_tensor_workspace_bytes():

@@ -204,6 +204,40 @@ nvfp4_status nvfp4_quantize_residual(const void* x, int64_t rows, int64_t cols, 
   return from_cuda(launch_quantize_residual(mode, p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+nvfp4_status nvfp4_row_amax(const void* x, int64_t rows, int64_t cols, float* row_amax,
+                            nvfp4_stream_t stream) {
+  if (rows < 0) return NVFP4_ERR_INVALID_ARG;
+  if (cols <= 0 || cols % kBlockElems != 0 || cols > (int64_t{1} << 30)) return NVFP4_ERR_SHAPE;
+  if (rows == 0) return NVFP4_OK;
+  if (x == nullptr || row_amax == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(row_amax, 4)) return NVFP4_ERR_ALIGNMENT;
+  if (overlap(x, 2 * static_cast<size_t>(rows * cols), row_amax, 4 * static_cast<size_t>(rows)))
+    return NVFP4_ERR_INVALID_ARG;
+  return from_cuda(launch_row_amax(static_cast<const uint16_t*>(x), rows, static_cast<int>(cols),
+                                   row_amax, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_quantize_guided(const void* x, int64_t rows, int64_t cols, nvfp4_mode mode,
+                                   const float* row_amax, const uint8_t* ref_codes,
+                                   const uint8_t* ref_block_scales, uint8_t* codes,
+                                   nvfp4_stream_t stream) {
+  if (!valid_mode(mode) || rows < 0) return NVFP4_ERR_INVALID_ARG;
+  if (cols <= 0 || cols % kBlockElems != 0 || cols > (int64_t{1} << 30)) return NVFP4_ERR_SHAPE;
+  if (rows == 0) return NVFP4_OK;
+  if (x == nullptr || row_amax == nullptr || ref_codes == nullptr || ref_block_scales == nullptr ||
+      codes == nullptr)
+    return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(row_amax, 4) || !aligned(ref_codes, 4) || !aligned(codes, 4))
+    return NVFP4_ERR_ALIGNMENT;
+  const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols);
+  if (overlap(codes, n / 2, x, 2 * n) || overlap(codes, n / 2, row_amax, 4 * static_cast<size_t>(rows)) ||
+      overlap(codes, n / 2, ref_codes, n / 2) || overlap(codes, n / 2, ref_block_scales, n / 16))
+    return NVFP4_ERR_INVALID_ARG;
+  GuidedParams p{static_cast<const uint16_t*>(x), rows, static_cast<int32_t>(cols), row_amax,
+                 ref_codes, ref_block_scales, codes};
+  return from_cuda(launch_quantize_guided(mode, p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t nvfp4_tensor_workspace_bytes(void) {
   return static_cast<size_t>(kAmaxMaxPartials) * sizeof(float);
 }

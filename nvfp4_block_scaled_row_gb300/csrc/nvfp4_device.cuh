@@ -67,6 +67,16 @@ struct QuantParams {
   uint64_t timeout_ns;      // bound on every barrier wait
 };
 
+struct GuidedParams {
+  const uint16_t* x;          // BF16 bits [rows][cols] (the trainer's values)
+  int64_t rows;
+  int32_t cols;
+  const float* row_amax;      // the rollout's per-token amax [rows]
+  const uint8_t* ref_codes;   // the rollout's codes [rows][cols/2]
+  const uint8_t* ref_scales;  // the rollout's E4M3 block scales [rows][cols/16]
+  uint8_t* codes;             // output codes [rows][cols/2]
+};
+
 struct DequantParams {
   const uint8_t* codes;
   const uint8_t* scales;

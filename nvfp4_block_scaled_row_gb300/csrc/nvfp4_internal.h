@@ -29,6 +29,13 @@ cudaError_t launch_quantize(int mode, bool tensor_scale, bool fused, QuantParams
 // (p.res_codes, p.res_scales, p.res_scale_out receive the residual's outputs).
 cudaError_t launch_quantize_residual(int mode, QuantParams p, cudaStream_t stream);
 
+// TRACE-guided codes (see GuidedParams).
+cudaError_t launch_quantize_guided(int mode, const GuidedParams& p, cudaStream_t stream);
+
+// amax[r] = max |x[r][k]| over each row.
+cudaError_t launch_row_amax(const uint16_t* x, int64_t rows, int cols, float* amax,
+                            cudaStream_t stream);
+
 // Whether the quantize kernels can stage a row of `cols` BF16 values.
 bool quantize_cols_supported(int64_t cols);
 

@@ -390,6 +390,90 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
   }
 }
 
+// TRACE rollout-guided rounding ("TRACE FP4 RL -- Rollout-guided FP4 rounding"): with the
+// rollout's per-token amax and block scales, each element's scaled value t is formed exactly as
+// the quantizer forms it; of its two neighbouring codewords the one closer to the rollout's
+// recorded codeword is kept.  Elementwise: warps walk rows, lane l owns 8-element group l of each
+// 256-element chunk.  The neighbours come from the hardware round-to-nearest code m of t: if the
+// rounding went away from zero they are (m-1, m), towards zero (m, m+1), none if t is on the grid
+// or saturated.  Of two adjacent magnitudes the larger is closer to the rollout's codeword exactly
+// when that codeword lies on t's side of zero with magnitude >= it.
+template <int kMode>
+__global__ void __launch_bounds__(256) guided_kernel(const GuidedParams p) {
+  __shared__ ScaleEntry tab[256];
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) tab[i] = make_scale_entry(i);
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t NW = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int cols = p.cols;
+  const int ngroups = cols / 8;
+  const uint16_t one_h = 0x3C00;  // FP16 1.0
+  for (int64_t row = gw; row < p.rows; row += NW) {
+    const RowFactors f = row_factors_warp<kMode>(p.row_amax[row], lane);
+    const f32x2 senc2 = pack2(f.S_enc, f.S_enc);
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + row * cols);
+    const uint32_t* rr = reinterpret_cast<const uint32_t*>(p.ref_codes + row * (cols / 2));
+    const uint8_t* sr = p.ref_scales + row * (cols / kBlockElems);
+    uint32_t* out = reinterpret_cast<uint32_t*>(p.codes + row * (cols / 2));
+    for (int g = lane; g < ngroups; g += 32) {
+      const uint4 xw = xr[g];
+      const uint32_t ref = rr[g];
+      const ScaleEntry e = tab[sr[g >> 1]];
+      const f32x2 inv2 = pack2(e.inv, e.inv);
+      f32x2 t[4];
+      t[0] = mul2(mul2(bf16x2_to_f32x2(xw.x), senc2), inv2);
+      t[1] = mul2(mul2(bf16x2_to_f32x2(xw.y), senc2), inv2);
+      t[2] = mul2(mul2(bf16x2_to_f32x2(xw.z), senc2), inv2);
+      t[3] = mul2(mul2(bf16x2_to_f32x2(xw.w), senc2), inv2);
+      uint32_t r[4];
+      const uint32_t rtn = e2m1x8_encode_decode(t[0], t[1], t[2], t[3], r);
+      // d = r - t per element (r exact in FP16, one rounding); its sign says which way t went.
+      float tv[8], dv[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        unpack2(t[j], tv[2 * j], tv[2 * j + 1]);
+        const f32x2 dd = fma_f16x2_f32x2(r[j], one_h | (one_h << 16), pack2(-tv[2 * j], -tv[2 * j + 1]));
+        unpack2(dd, dv[2 * j], dv[2 * j + 1]);
+      }
+      uint32_t word = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float ti = tv[i], d = dv[i];
+        const uint32_t code = (rtn >> (4 * i)) & 0xFu;
+        const uint32_t m = code & 7u, sign = code >> 3;
+        const bool away = (d > 0.0f && ti > 0.0f) || (d < 0.0f && ti < 0.0f);
+        const uint32_t m_lo = away ? m - 1 : m;
+        const uint32_t m_hi = (d == 0.0f || away) ? m : min(m + 1, 7u);
+        const uint32_t rc = (ref >> (4 * i)) & 0xFu;
+        const bool take_hi = m_hi != m_lo && (rc >> 3) == sign && (rc & 7u) >= m_hi;
+        word |= ((sign << 3) | (take_hi ? m_hi : m_lo)) << (4 * i);
+      }
+      out[g] = word;
+    }
+  }
+}
+
+// Per-row amax max |x| over each row of `cols` BF16 values (warp per row).
+__global__ void __launch_bounds__(256) row_amax_kernel(const uint16_t* x, int64_t rows, int cols,
+                                                       float* amax) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t NW = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t row = gw; row < rows; row += NW) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * cols);
+    uint32_t m2 = 0;
+    for (int g = lane; g < cols / 8; g += 32) {
+      const uint4 v = __ldcs(xr + g);
+      m2 = max_abs_bf16x2(m2, max_abs_bf16x2(max_abs_bf16x2(v.x, v.y), max_abs_bf16x2(v.z, v.w)));
+    }
+    float a = abs_max_of_pair(m2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+    if (lane == 0) amax[row] = a;
+  }
+}
+
 struct RingShape {
   int warps;
   int stages;
@@ -522,6 +606,36 @@ cudaError_t launch_quantize(int mode, bool tensor_scale, bool fused, QuantParams
                  : launch_impl<kModeSix, true, false, false>(p, stream);
   return fused ? launch_impl<kModeSix, false, true, false>(p, stream)
                : launch_impl<kModeSix, false, false, false>(p, stream);
+}
+
+cudaError_t launch_quantize_guided(int mode, const GuidedParams& p, cudaStream_t stream) {
+  int device = 0;
+  cudaError_t err = cudaGetDevice(&device);
+  if (err != cudaSuccess) return err;
+  int64_t grid = (p.rows + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(sm_count(device)) * 8;
+  if (grid > cap) grid = cap;
+  const LaunchOverride ov = launch_override();
+  if (ov.max_ctas > 0 && grid > ov.max_ctas) grid = ov.max_ctas;
+  if (grid < 1) grid = 1;
+  if (mode == kModeFourOverSix)
+    guided_kernel<kModeFourOverSix><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
+  else
+    guided_kernel<kModeSix><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_amax(const uint16_t* x, int64_t rows, int cols, float* amax,
+                            cudaStream_t stream) {
+  int device = 0;
+  cudaError_t err = cudaGetDevice(&device);
+  if (err != cudaSuccess) return err;
+  int64_t grid = (rows + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(sm_count(device)) * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  row_amax_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(x, rows, cols, amax);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_residual(int mode, QuantParams p, cudaStream_t stream) {

@@ -51,6 +51,8 @@ def _load():
     lib.oracle_quantize_given_amax.argtypes = [P, I64, I64, I, ctypes.c_float, P, P, P]
     lib.oracle_quantize_residual.restype = I
     lib.oracle_quantize_residual.argtypes = [P, I64, I64, I, P, P, P, P, P, P]
+    lib.oracle_quantize_guided.restype = I
+    lib.oracle_quantize_guided.argtypes = [P, I64, I64, I, P, P, P, P]
     lib.oracle_dequantize.restype = I
     lib.oracle_dequantize.argtypes = [P, P, P, I, I64, I64, P]
     for name in ("oracle_e2m1_encode_array", "oracle_e4m3_encode_array",
@@ -174,6 +176,21 @@ def quantize_residual(x_u16, mode=MODE_FOUR_OVER_SIX):
     if rc:
         raise ValueError("oracle_quantize_residual rejected its arguments")
     return a, b
+
+
+def quantize_guided(x_u16, row_amax, ref_codes, ref_scales, mode=MODE_FOUR_OVER_SIX):
+    """TRACE-guided codes for x given the rollout's per-token amax, codes and block scales."""
+    x = _u16(x_u16)
+    rows, cols = x.shape
+    row_amax = np.ascontiguousarray(row_amax, np.float32)
+    ref_codes = np.ascontiguousarray(ref_codes, np.uint8)
+    ref_scales = np.ascontiguousarray(ref_scales, np.uint8)
+    out = np.zeros((rows, cols // 2), np.uint8)
+    rc = _load().oracle_quantize_guided(_ptr(x), rows, cols, int(mode), _ptr(row_amax),
+                                        _ptr(ref_codes), _ptr(ref_scales), _ptr(out))
+    if rc:
+        raise ValueError("oracle_quantize_guided rejected its arguments")
+    return out
 
 
 def dequantize(codes, scales, scale, scale_kind=SCALE_ROW):

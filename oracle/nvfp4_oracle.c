@@ -342,6 +342,47 @@ int oracle_quantize_residual(const uint16_t* x, int64_t rows, int64_t cols, int 
   return 0;
 }
 
+/* TRACE rollout-guided rounding ("TRACE FP4 RL -- Rollout-guided FP4 rounding": between the two
+ * neighbouring codewords of its own scaled value, the trainer picks the one closest to the
+ * codeword the rollout recorded, using the rollout-side scale).  The scale comes from the
+ * rollout: its per-token amax (row_amax, one float per row) gives S_enc as in the quantizer, and
+ * its E4M3 block scale bytes give s.  t is formed exactly as the quantizer forms it.  The
+ * neighbours are lo = the largest signed grid value <= t and hi = the smallest >= t, with t
+ * beyond +-6 saturating to +-6; the output is whichever of lo, hi lies closer to the rollout's
+ * value (they coincide when t is on the grid).  A zero output keeps the sign of t. */
+int oracle_quantize_guided(const uint16_t* x, int64_t rows, int64_t cols, int mode,
+                           const float* row_amax, const uint8_t* ref_codes,
+                           const uint8_t* ref_scales, uint8_t* codes_out) {
+  if (check_shape(rows, cols, mode)) return 1;
+  static const double grid[15] = {-6, -4, -3, -2, -1.5, -1, -0.5, 0, 0.5, 1, 1.5, 2, 3, 4, 6};
+  int64_t nb = cols / ORACLE_BLOCK;
+  for (int64_t r = 0; r < rows; ++r) {
+    float f[4];
+    oracle_factors(row_amax[r], mode, f);
+    for (int64_t k = 0; k < cols; ++k) {
+      float s = (float)oracle_e4m3_value(ref_scales[r * nb + k / ORACLE_BLOCK]);
+      float inv = (s == 0.0f) ? 0.0f : 1.0f / s;
+      float z = oracle_bf16_to_f32(x[r * cols + k]) * f[0];
+      float t = z * inv;
+      double tc = t > 6.0f ? 6.0 : (t < -6.0f ? -6.0 : (double)t);
+      double lo = grid[0], hi = grid[14];
+      for (int g = 0; g < 15; ++g) {
+        if (grid[g] <= tc) lo = grid[g];
+        if (grid[14 - g] >= tc) hi = grid[14 - g];
+      }
+      uint8_t byte = ref_codes[r * (cols / 2) + k / 2];
+      int ref = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+      double rv = oracle_e2m1_value(ref);
+      double v = (fabs(hi - rv) < fabs(lo - rv)) ? hi : lo;
+      int code = oracle_e2m1_encode((float)v);
+      if (v == 0.0) code = signbit(t) ? 8 : 0;
+      uint8_t* out = &codes_out[r * (cols / 2) + k / 2];
+      *out = (k % 2 == 0) ? (uint8_t)((*out & 0xF0) | code) : (uint8_t)((*out & 0x0F) | (code << 4));
+    }
+  }
+  return 0;
+}
+
 /* Array forms of the format conversions, for the format tests. */
 void oracle_e2m1_encode_array(const float* t, int64_t n, uint8_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)oracle_e2m1_encode(t[i]);

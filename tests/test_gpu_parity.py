@@ -347,3 +347,41 @@ def test_residual_edge_values(cols):
 def test_residual_full_size_sampled():
     x = synth.generate(2, device=DEV)["x"]
     check_residual(x, F4, _sample_rows(x.shape[0], n=32, seed=7))
+
+
+
+def _perturbed(x, seed):
+    """The training engine's view of the rollout's activations: a few BF16 ulps of noise."""
+    g = torch.Generator(device=x.device).manual_seed(seed)
+    noise = torch.randn(x.shape, generator=g, device=x.device) * 2.0 ** -7
+    return (x.float() * (1 + noise)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("index,rows", [(0, None), (2, 256), (4, 300)])
+def test_guided_rounding_matches_oracle(index, rows):
+    x_roll = synth.generate(index, device=DEV, rows=rows)["x"]
+    amax = nv.nvfp4_row_amax(x_roll)
+    xb = synth.as_u16(x_roll)
+    assert np.array_equal(_np(amax), np.array([oracle.amax(xb[r]) for r in range(xb.shape[0])],
+                                              np.float32))
+    codes, scales, _ = nv.nvfp4_quantize_rowwise(x_roll)
+    same = nv.nvfp4_quantize_guided(x_roll, amax, codes, scales)
+    assert torch.equal(same, codes)  # trainer == rollout -> the rollout's codes
+    x_tr = _perturbed(x_roll, index)
+    got = nv.nvfp4_quantize_guided(x_tr, amax, codes, scales)
+    want = oracle.quantize_guided(synth.as_u16(x_tr), _np(amax), _np(codes), _np(scales))
+    _assert_equal(_np(got), want, "guided codes")
+    own = nv.nvfp4_quantize_guided(x_tr, amax, got, scales)  # idempotent on its own output
+    assert torch.equal(own, got)
+    assert nv.nvfp4_get_device_status() == 0
+
+
+@pytest.mark.parametrize("cols", [16, 48, 7184])
+def test_guided_rounding_edge_values(cols):
+    x_roll = _edge_matrix(16, cols, seed=cols + 3)
+    amax = nv.nvfp4_row_amax(x_roll)
+    codes, scales, _ = nv.nvfp4_quantize_rowwise(x_roll)
+    x_tr = _perturbed(x_roll, cols)
+    got = nv.nvfp4_quantize_guided(x_tr, amax, codes, scales)
+    want = oracle.quantize_guided(synth.as_u16(x_tr), _np(amax), _np(codes), _np(scales))
+    _assert_equal(_np(got), want, "guided codes (edge)")
