@@ -26,7 +26,7 @@
  *   block_scales  uint8 [rows][cols/16]: one FP8 E4M3 byte per 16-element block.
  *   row scale     float [rows]: S_dec = amax_row / (6 * M) per row.
  *   tensor scale  float [1]:    S_dec = amax_tensor / (6 * M).
- *   M = 256 in mode FOUR_OVER_SIX and 448 in mode SIX.
+ *   M = 256 in modes FOUR_OVER_SIX and FOUR_OVER_SIX_FP16, 448 in mode SIX.
  *
  * Contract common to every call:
  *   - Asynchronous on `stream` (NULL = the legacy default stream); nothing synchronizes.
@@ -54,7 +54,13 @@ typedef struct CUstream_st* nvfp4_stream_t;
 
 typedef enum {
   NVFP4_MODE_SIX = 0,           /* block max always mapped to +-6 (ordinary NVFP4)           */
-  NVFP4_MODE_FOUR_OVER_SIX = 1  /* block max mapped to +-6 or +-4, lower block error wins    */
+  NVFP4_MODE_FOUR_OVER_SIX = 1, /* block max mapped to +-6 or +-4, lower block error wins    */
+  /* As FOUR_OVER_SIX, but the two block errors are computed and compared in FP16 arithmetic
+   * (the fast path of "NVFP4 RL" Sec. 4, "The optimization"): the target is scaled down by the
+   * candidate's scale and cast to FP16, residuals and their squares are summed in FP16, and the
+   * sums are brought to a common scale in FP32 (E * s^2).  Same candidates and codes as
+   * FOUR_OVER_SIX; only near-tie choices can differ. */
+  NVFP4_MODE_FOUR_OVER_SIX_FP16 = 2
 } nvfp4_mode;
 
 typedef enum {

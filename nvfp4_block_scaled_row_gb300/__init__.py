@@ -25,10 +25,12 @@ __all__ = [
 
 MODE_SIX = 0
 MODE_FOUR_OVER_SIX = 1
+MODE_FOUR_OVER_SIX_FP16 = 2
 SCALE_ROW = 0
 SCALE_TENSOR = 1
-_MODES = {"six": MODE_SIX, "four_over_six": MODE_FOUR_OVER_SIX, MODE_SIX: MODE_SIX,
-          MODE_FOUR_OVER_SIX: MODE_FOUR_OVER_SIX}
+_MODES = {"six": MODE_SIX, "four_over_six": MODE_FOUR_OVER_SIX,
+          "four_over_six_fp16": MODE_FOUR_OVER_SIX_FP16, MODE_SIX: MODE_SIX,
+          MODE_FOUR_OVER_SIX: MODE_FOUR_OVER_SIX, MODE_FOUR_OVER_SIX_FP16: MODE_FOUR_OVER_SIX_FP16}
 _KINDS = {"row": SCALE_ROW, "tensor": SCALE_TENSOR, SCALE_ROW: SCALE_ROW,
           SCALE_TENSOR: SCALE_TENSOR}
 

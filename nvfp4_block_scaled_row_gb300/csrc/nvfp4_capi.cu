@@ -34,7 +34,10 @@ bool overlap(const void* a, size_t an, const void* b, size_t bn) {
   return a0 < b0 + bn && b0 < a0 + an;
 }
 
-bool valid_mode(int mode) { return mode == NVFP4_MODE_SIX || mode == NVFP4_MODE_FOUR_OVER_SIX; }
+bool valid_mode(int mode) {
+  return mode == NVFP4_MODE_SIX || mode == NVFP4_MODE_FOUR_OVER_SIX ||
+         mode == NVFP4_MODE_FOUR_OVER_SIX_FP16;
+}
 bool valid_kind(int kind) { return kind == NVFP4_SCALE_ROW || kind == NVFP4_SCALE_TENSOR; }
 
 // The status word's device address for the current device (looked up once per device).

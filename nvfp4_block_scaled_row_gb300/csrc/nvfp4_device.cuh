@@ -36,6 +36,7 @@ constexpr int kStatusOffsets = 6;
 // Mode numbers (same as nvfp4_mode).
 constexpr int kModeSix = 0;
 constexpr int kModeFourOverSix = 1;
+constexpr int kModeFourOverSixFp16 = 2;  // 4/6 with the block errors compared in FP16 arithmetic
 
 // Per E4M3 byte: the correctly rounded reciprocal of its value s (0 for s == 0) and -s as an
 // FP16 pair (E4M3 values are exact in FP16).
@@ -315,6 +316,49 @@ __device__ __forceinline__ f32x2 fma_f16x2_f32x2(uint32_t a, uint32_t b, f32x2 c
       : "=f"(d0), "=f"(d1)
       : "r"(a), "r"(b), "f"(c0), "f"(c1));
   return pack2(d0, d1);
+}
+
+// FP32 pair to FP16 pair (RNE): .x to the low half.
+__device__ __forceinline__ uint32_t f16x2_from_f32x2(f32x2 v) {
+  float lo, hi;
+  unpack2(v, lo, hi);
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Per half: a - b in FP16 (RNE).
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Per half: d*d + acc as one FP16 fused multiply-add (RNE).
+__device__ __forceinline__ uint32_t fma_f16x2(uint32_t d, uint32_t acc) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %1, %2;" : "=r"(r) : "r"(d), "r"(acc));
+  return r;
+}
+
+// f16(f16(a.lo + a.hi) + f16(b.lo + b.hi)) as FP32 (exact widening).
+__device__ __forceinline__ float f16_sum_of_halves(uint32_t a, uint32_t b) {
+  float r;
+  asm("{\n\t.reg .f16 al, ah, bl, bh, sa, sb, s;\n\t"
+      "mov.b32 {al, ah}, %1;\n\t"
+      "mov.b32 {bl, bh}, %2;\n\t"
+      "add.rn.f16 sa, al, ah;\n\t"
+      "add.rn.f16 sb, bl, bh;\n\t"
+      "add.rn.f16 s, sa, sb;\n\t"
+      "cvt.f32.f16 %0, s;\n\t}"
+      : "=f"(r)
+      : "r"(a), "r"(b));
+  return r;
+}
+
+// The low FP16 half of a word, widened exactly to FP32.
+__device__ __forceinline__ float f16_low_to_f32(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
 }
 
 // FP32 pair to BF16 pair (RNE): .x to the low half.

@@ -54,7 +54,9 @@ extern "C" nvfp4_status nvfp4_fused_roundtrip_host(const void* x, int64_t rows, 
                                                    void* y, void* workspace,
                                                    size_t workspace_bytes,
                                                    nvfp4_stream_t stream) {
-  if ((mode != NVFP4_MODE_SIX && mode != NVFP4_MODE_FOUR_OVER_SIX) || rows < 0)
+  if ((mode != NVFP4_MODE_SIX && mode != NVFP4_MODE_FOUR_OVER_SIX &&
+       mode != NVFP4_MODE_FOUR_OVER_SIX_FP16) ||
+      rows < 0)
     return NVFP4_ERR_INVALID_ARG;
   if (cols <= 0 || cols % nvfp4::kBlockElems != 0 || !nvfp4::quantize_cols_supported(cols))
     return NVFP4_ERR_SHAPE;

@@ -35,7 +35,7 @@ struct RowFactors {
 // clamped to FLT_MAX when it overflows; a zero amax gives all-zero factors.
 template <int kMode>
 __device__ __forceinline__ RowFactors row_factors(float a) {
-  constexpr float M = (kMode == kModeFourOverSix) ? 256.0f : 448.0f;
+  constexpr float M = (kMode == kModeSix) ? 448.0f : 256.0f;
   RowFactors f;
   if (a == 0.0f) {
     f.S_enc = f.c6 = f.c4 = f.S_dec = 0.0f;
@@ -52,7 +52,7 @@ __device__ __forceinline__ RowFactors row_factors(float a) {
 // (lanes 0-3) and broadcast; identical results to row_factors.
 template <int kMode>
 __device__ __forceinline__ RowFactors row_factors_warp(float a, int lane) {
-  constexpr float M = (kMode == kModeFourOverSix) ? 256.0f : 448.0f;
+  constexpr float M = (kMode == kModeSix) ? 448.0f : 256.0f;
   const float num = lane == 0 ? 6.0f * M : (lane == 1 ? M : (lane == 2 ? 1.5f * M : a));
   const float den = lane == 3 ? 6.0f * M : a;
   float q = __fdiv_rn(num, den);
@@ -103,6 +103,34 @@ __device__ __forceinline__ Candidate encode_candidate(const f32x2 (&z)[8], const
   return c;
 }
 
+// The FP16 reading of the 4/6 fast path ("NVFP4 RL" blog, Sec. 4, "The optimization": cast to
+// FP16 losslessly and scale the target down by its inverse): the same targets and codes as
+// encode_candidate, but the block error is taken in FP16 in the scaled-down domain,
+//   delta = f16(f16(t) - r),  E[h][p] = FP16 FMA chains,  E = f16(f16(EA0 + EA1) + f16(EB0 + EB1)),
+// and brought back to a common scale in FP32 as fp32(E) * s^2 (s^2 exact).
+__device__ __forceinline__ Candidate encode_candidate_fp16(const f32x2 (&z)[8], const ScaleEntry e) {
+  Candidate c;
+  const f32x2 inv2 = pack2(e.inv, e.inv);
+  f32x2 t[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) t[j] = mul2(z[j], inv2);
+  uint32_t rA[4], rB[4];
+  c.cw[0] = e2m1x8_encode_decode(t[0], t[1], t[2], t[3], rA);
+  c.cw[1] = e2m1x8_encode_decode(t[4], t[5], t[6], t[7], rB);
+  uint32_t accA = 0u, accB = 0u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    accA = fma_f16x2(sub_f16x2(f16x2_from_f32x2(t[j]), rA[j]), accA);
+    accB = fma_f16x2(sub_f16x2(f16x2_from_f32x2(t[4 + j]), rB[j]), accB);
+    c.r[j] = rA[j];
+    c.r[4 + j] = rB[j];
+  }
+  const float E = f16_sum_of_halves(accA, accB);
+  const float s = -f16_low_to_f32(e.neg_s_h2);
+  c.err = __fmul_rn(E, __fmul_rn(s, s));
+  return c;
+}
+
 // Encodes one 16-element block with block amax m: both candidates (scale-to-6 only in mode six),
 // the 4/6 choice, then stores the 8 code bytes and the E4M3 scale byte.  Half A holds elements
 // 8*h0 .. 8*h0+7 of the block, half B the other eight.  With kWantY, `out` receives the block's
@@ -116,7 +144,7 @@ __device__ __forceinline__ void encode_block(const uint4 A, const uint4 B, float
   const uint16_t one_bf16 = 0x3F80;
   const float neg_zero = -0.0f;
   const float u6 = __fmul_rn(m, f.c6);
-  const float u4 = (kMode == kModeFourOverSix) ? __fmul_rn(m, f.c4) : 0.0f;
+  const float u4 = (kMode != kModeSix) ? __fmul_rn(m, f.c4) : 0.0f;
   const uint32_t sb = e4m3x2_from_f32(u4, u6);
   const uint32_t b6 = sb & 0xFFu, b4 = sb >> 8;
 
@@ -131,13 +159,14 @@ __device__ __forceinline__ void encode_block(const uint4 A, const uint4 B, float
   z[7] = mul2(bf16x2_to_f32x2_fma(B.w, one_bf16, neg_zero), senc2);
 
   const ScaleEntry e6 = tab[b6];
-  const Candidate c6 = encode_candidate(z, e6);
+  const Candidate c6 =
+      (kMode == kModeFourOverSixFp16) ? encode_candidate_fp16(z, e6) : encode_candidate(z, e6);
   bool pick4 = false;
   Candidate c4{};
   ScaleEntry e4{};
-  if (kMode == kModeFourOverSix) {
+  if (kMode != kModeSix) {
     e4 = tab[b4];
-    c4 = encode_candidate(z, e4);
+    c4 = (kMode == kModeFourOverSixFp16) ? encode_candidate_fp16(z, e4) : encode_candidate(z, e4);
     pick4 = c4.err < c6.err;  // ties go to 6
   }
   uint32_t* cw = reinterpret_cast<uint32_t*>(codes_blk);
@@ -592,20 +621,23 @@ bool quantize_cols_supported(int64_t cols) {
   return cols > 0 && cols <= kMaxCols && cols % kBlockElems == 0 && choose_ring(cols, &rs);
 }
 
+template <int kMode>
+cudaError_t launch_mode(bool tensor_scale, bool fused, QuantParams p, cudaStream_t stream) {
+  if (tensor_scale)
+    return fused ? launch_impl<kMode, true, true, false>(p, stream)
+                 : launch_impl<kMode, true, false, false>(p, stream);
+  return fused ? launch_impl<kMode, false, true, false>(p, stream)
+               : launch_impl<kMode, false, false, false>(p, stream);
+}
+
 cudaError_t launch_quantize(int mode, bool tensor_scale, bool fused, QuantParams p,
                             cudaStream_t stream) {
-  if (mode == kModeFourOverSix) {
-    if (tensor_scale)
-      return fused ? launch_impl<kModeFourOverSix, true, true, false>(p, stream)
-                   : launch_impl<kModeFourOverSix, true, false, false>(p, stream);
-    return fused ? launch_impl<kModeFourOverSix, false, true, false>(p, stream)
-                 : launch_impl<kModeFourOverSix, false, false, false>(p, stream);
+  switch (mode) {
+    case kModeFourOverSix: return launch_mode<kModeFourOverSix>(tensor_scale, fused, p, stream);
+    case kModeFourOverSixFp16:
+      return launch_mode<kModeFourOverSixFp16>(tensor_scale, fused, p, stream);
+    default: return launch_mode<kModeSix>(tensor_scale, fused, p, stream);
   }
-  if (tensor_scale)
-    return fused ? launch_impl<kModeSix, true, true, false>(p, stream)
-                 : launch_impl<kModeSix, true, false, false>(p, stream);
-  return fused ? launch_impl<kModeSix, false, true, false>(p, stream)
-               : launch_impl<kModeSix, false, false, false>(p, stream);
 }
 
 cudaError_t launch_quantize_guided(int mode, const GuidedParams& p, cudaStream_t stream) {
@@ -618,10 +650,11 @@ cudaError_t launch_quantize_guided(int mode, const GuidedParams& p, cudaStream_t
   const LaunchOverride ov = launch_override();
   if (ov.max_ctas > 0 && grid > ov.max_ctas) grid = ov.max_ctas;
   if (grid < 1) grid = 1;
-  if (mode == kModeFourOverSix)
-    guided_kernel<kModeFourOverSix><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
-  else
+  // The guided encoder keeps the rollout's scales: only M (mode six or not) matters.
+  if (mode == kModeSix)
     guided_kernel<kModeSix><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
+  else
+    guided_kernel<kModeFourOverSix><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -639,8 +672,12 @@ cudaError_t launch_row_amax(const uint16_t* x, int64_t rows, int cols, float* am
 }
 
 cudaError_t launch_quantize_residual(int mode, QuantParams p, cudaStream_t stream) {
-  return mode == kModeFourOverSix ? launch_impl<kModeFourOverSix, false, false, true>(p, stream)
-                                  : launch_impl<kModeSix, false, false, true>(p, stream);
+  switch (mode) {
+    case kModeFourOverSix: return launch_impl<kModeFourOverSix, false, false, true>(p, stream);
+    case kModeFourOverSixFp16:
+      return launch_impl<kModeFourOverSixFp16, false, false, true>(p, stream);
+    default: return launch_impl<kModeSix, false, false, true>(p, stream);
+  }
 }
 
 }  // namespace nvfp4

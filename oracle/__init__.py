@@ -15,6 +15,7 @@ from . import build as _build
 
 MODE_SIX = 0
 MODE_FOUR_OVER_SIX = 1
+MODE_FOUR_OVER_SIX_FP16 = 2
 SCALE_ROW = 0
 SCALE_TENSOR = 1
 BLOCK = 16
@@ -51,6 +52,8 @@ def _load():
     lib.oracle_quantize_given_amax.argtypes = [P, I64, I64, I, ctypes.c_float, P, P, P]
     lib.oracle_quantize_residual.restype = I
     lib.oracle_quantize_residual.argtypes = [P, I64, I64, I, P, P, P, P, P, P]
+    lib.oracle_f16_round_array.restype = None
+    lib.oracle_f16_round_array.argtypes = [P, I64, P]
     lib.oracle_quantize_guided.restype = I
     lib.oracle_quantize_guided.argtypes = [P, I64, I64, I, P, P, P, P]
     lib.oracle_dequantize.restype = I
@@ -102,6 +105,14 @@ def bf16_encode(v):
     v = np.ascontiguousarray(v, dtype=np.float32)
     out = np.empty(v.shape, np.uint16)
     _load().oracle_bf16_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def f16_round(v):
+    """The oracle's FP16 round-to-nearest-even of float64 values."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, np.float64)
+    _load().oracle_f16_round_array(_ptr(v), v.size, _ptr(out))
     return out
 
 

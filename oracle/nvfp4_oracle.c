@@ -50,6 +50,7 @@
 
 #define ORACLE_MODE_SIX 0
 #define ORACLE_MODE_FOUR_OVER_SIX 1
+#define ORACLE_MODE_FOUR_OVER_SIX_FP16 2
 #define ORACLE_SCALE_ROW 0
 #define ORACLE_SCALE_TENSOR 1
 #define ORACLE_BLOCK 16
@@ -141,13 +142,27 @@ uint16_t oracle_bf16_encode(float v) {
   return (uint16_t)((((lo >> 16) & 1u) != 0) ? (hi >> 16) : (lo >> 16));
 }
 
+/* IEEE binary16 round-to-nearest-even of a double: 11 significant bits, subnormal quantum 2^-24,
+ * magnitudes at or past 65520 (the midpoint above the largest finite, 65504) become infinity. */
+double oracle_f16_round(double v) {
+  if (isnan(v)) return v;
+  double a = fabs(v);
+  if (a >= 65520.0) return copysign(INFINITY, v);
+  if (a == 0.0) return v;
+  int e;
+  frexp(a, &e);                            /* a = f * 2^e, f in [0.5, 1) */
+  int q = (e - 1 < -14) ? -24 : (e - 1) - 10; /* quantum exponent */
+  double r = ldexp(rint(ldexp(a, -q)), q);  /* rint: ties to even in the default rounding mode */
+  return copysign(r, v);
+}
+
 /* ------------------------------------------------------------------------------------------------
  * The method.
  * ---------------------------------------------------------------------------------------------- */
 
 /* E4M3_4OVER6_MAXVAL of the 4/6 candidate formula ([RL-blog] Sec. 4); the page names it without a
  * value.  256 keeps 1.5*M <= 448, so the scale-to-4 candidate never saturates. */
-static float oracle_mode_max(int mode) { return mode == ORACLE_MODE_FOUR_OVER_SIX ? 256.0f : 448.0f; }
+static float oracle_mode_max(int mode) { return mode == ORACLE_MODE_SIX ? 448.0f : 256.0f; }
 
 static float clamp_to_finite(float v) { return v > FLT_MAX ? FLT_MAX : v; }
 
@@ -197,6 +212,36 @@ static int quantize_candidate(const float x[ORACLE_BLOCK], float m, float S_enc,
   return sbyte;
 }
 
+/* The FP16 reading of the 4/6 fast path ([RL-blog] Sec. 4, "The optimization": cast losslessly
+ * to FP16 and scale the target down by its inverse instead of scaling the candidate up): the same
+ * scaled targets t and codes as the FP32 candidate, the target cast to FP16, the residual
+ * delta = f16(f16(t) - r) (r exact in FP16), two FP16 FMA chains per half (elements 8h+p+2k,
+ * k ascending), E = f16(f16(E[0][0] + E[0][1]) + f16(E[1][0] + E[1][1])), and the error brought
+ * back to the common scale in FP32: e = fp32(E) * (s*s) (s*s exact). */
+static float candidate_error_fp16(const float x[ORACLE_BLOCK], float S_enc, float s,
+                                  const uint8_t code[ORACLE_BLOCK]) {
+  float inv = (s == 0.0f) ? 0.0f : 1.0f / s;
+  double d[ORACLE_BLOCK];
+  for (int i = 0; i < ORACLE_BLOCK; ++i) {
+    float z = x[i] * S_enc;
+    float t = z * inv;
+    double th = oracle_f16_round((double)t);
+    d[i] = oracle_f16_round(th - oracle_e2m1_value(code[i]));
+  }
+  double E[2][2];
+  for (int h = 0; h < 2; ++h)
+    for (int p = 0; p < 2; ++p) {
+      double acc = 0.0;
+      for (int k = 0; k < 4; ++k) {
+        double di = d[8 * h + p + 2 * k];
+        acc = oracle_f16_round(di * di + acc); /* one FP16 fma: exact in double, one rounding */
+      }
+      E[h][p] = acc;
+    }
+  double Eh = oracle_f16_round(oracle_f16_round(E[0][0] + E[0][1]) + oracle_f16_round(E[1][0] + E[1][1]));
+  return (float)Eh * (s * s);
+}
+
 /* One block: both candidates (only scale-to-6 in mode six), then the 4/6 choice ([RL-blog] Sec. 4).
  * Writes 8 packed code bytes and the scale byte; returns 1 when scale-to-4 was chosen. */
 static int quantize_block(const float x[ORACLE_BLOCK], const float f[4], int mode,
@@ -211,6 +256,11 @@ static int quantize_block(const float x[ORACLE_BLOCK], const float f[4], int mod
   if (mode == ORACLE_MODE_FOUR_OVER_SIX) {
     s4 = quantize_candidate(x, m, f[0], f[2], c4, &e4);
     pick4 = e4 < e6; /* ties go to 6 */
+  } else if (mode == ORACLE_MODE_FOUR_OVER_SIX_FP16) {
+    s4 = quantize_candidate(x, m, f[0], f[2], c4, &e4);
+    e6 = candidate_error_fp16(x, f[0], (float)oracle_e4m3_value(s6), c6);
+    e4 = candidate_error_fp16(x, f[0], (float)oracle_e4m3_value(s4), c4);
+    pick4 = e4 < e6;
   }
   const uint8_t* c = pick4 ? c4 : c6;
   for (int j = 0; j < ORACLE_BLOCK / 2; ++j) packed[j] = (uint8_t)(c[2 * j] | (c[2 * j + 1] << 4));
@@ -228,7 +278,9 @@ float oracle_amax(const uint16_t* x, int64_t n) {
 
 static int check_shape(int64_t rows, int64_t cols, int mode) {
   if (rows < 0 || cols <= 0 || cols % ORACLE_BLOCK != 0) return 1;
-  if (mode != ORACLE_MODE_SIX && mode != ORACLE_MODE_FOUR_OVER_SIX) return 1;
+  if (mode != ORACLE_MODE_SIX && mode != ORACLE_MODE_FOUR_OVER_SIX &&
+      mode != ORACLE_MODE_FOUR_OVER_SIX_FP16)
+    return 1;
   return 0;
 }
 
@@ -390,6 +442,10 @@ void oracle_e2m1_encode_array(const float* t, int64_t n, uint8_t* out) {
 
 void oracle_e4m3_encode_array(const float* v, int64_t n, uint8_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)oracle_e4m3_encode(v[i]);
+}
+
+void oracle_f16_round_array(const double* v, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_f16_round(v[i]);
 }
 
 void oracle_bf16_encode_array(const float* v, int64_t n, uint16_t* out) {

@@ -16,8 +16,8 @@ from nvfp4_block_scaled_row_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-F4, SIX = "four_over_six", "six"
-OMODE = {F4: oracle.MODE_FOUR_OVER_SIX, SIX: oracle.MODE_SIX}
+F4, SIX, F16 = "four_over_six", "six", "four_over_six_fp16"
+OMODE = {F4: oracle.MODE_FOUR_OVER_SIX, SIX: oracle.MODE_SIX, F16: oracle.MODE_FOUR_OVER_SIX_FP16}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -385,3 +385,20 @@ def test_guided_rounding_edge_values(cols):
     got = nv.nvfp4_quantize_guided(x_tr, amax, codes, scales)
     want = oracle.quantize_guided(synth.as_u16(x_tr), _np(amax), _np(codes), _np(scales))
     _assert_equal(_np(got), want, "guided codes (edge)")
+
+
+
+@pytest.mark.parametrize("index,rows", [(0, None), (2, 300), (3, 640), (4, 500)])
+def test_fp16_selector_mode(index, rows):
+    """The FP16 reading of the 4/6 fast path is bit-exact against its oracle statement too."""
+    x = synth.generate(index, device=DEV, rows=rows)["x"]
+    check_rowwise(x, F16)
+    check_residual(x, F16)
+    if index == 0:
+        check_tensor(x, F16)
+
+
+def test_fp16_selector_edge_values():
+    x = _edge_matrix(37, 7184, seed=11)
+    check_rowwise(x, F16)
+    check_tensor(x[:9].contiguous(), F16)
