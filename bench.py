@@ -272,6 +272,21 @@ def bench_op(nv, x, op, kind, mode, steps, warmup, world, device, offsets=None):
         fn = lambda: nv.nvfp4_quantize_tensor(x, mode, codes, scales, scale, ws)
     elif op == "residual":
         fn = lambda: nv.nvfp4_quantize_residual(x, mode)
+    elif op == "gemm":  # y = x . w^T, w = the first 2048 rows of the weight workload
+        from nvfp4_block_scaled_row_gb300 import synth
+        w = synth.generate(1, device=device)["x"][:, :cols].contiguous()
+        xc, xs, xd = nv.nvfp4_quantize_rowwise(x, mode)
+        wc, ws, wd = nv.nvfp4_quantize_tensor(w, mode)
+        xsw, wsw = nv.nvfp4_swizzle_block_scales(xs, cols), nv.nvfp4_swizzle_block_scales(ws, cols)
+        y = torch.empty((rows, w.shape[0]), dtype=torch.bfloat16, device=device)
+        ws_buf = torch.empty(nv.nvfp4_gemm_workspace_bytes(rows, w.shape[0]), dtype=torch.uint8,
+                             device=device)
+        fn = lambda: nv.nvfp4_gemm_nt(xc, xsw, xd, wc, wsw, wd, y, ws_buf)
+        per, region = time_steps(fn, steps, warmup, world, device)
+        ms = statistics.mean(per)
+        flops = 2.0 * rows * w.shape[0] * cols
+        return {"gbs": flops / (ms * 1e-3) / 1e12, "ms": ms, "region_ms": region,
+                "launches_per_step": 2, "unit": "TFLOP/s"}
     elif op == "guided":
         amax = nv.nvfp4_row_amax(x)
         rc, rs, _ = nv.nvfp4_quantize_rowwise(x, mode)
@@ -361,7 +376,8 @@ def main():
                      d["offsets"] if op == "quantize" and kind == "row" else None)
         if rank == 0:
             print(json.dumps({"only": args.only, "shape": list(d["x"].shape),
-                              "us_per_step": round(r["ms"] * 1e3, 2), "gbs": round(r["gbs"], 1),
+                              "us_per_step": round(r["ms"] * 1e3, 2),
+                              r.get("unit", "gbs"): round(r["gbs"], 1),
                               "device_status": nv.nvfp4_get_device_status()}))
         if world > 1:
             torch.distributed.destroy_process_group()

@@ -208,6 +208,38 @@ nvfp4_status nvfp4_fused_roundtrip_host(const void* x, int64_t rows, int64_t col
                                         float* row_scale, void* y, void* workspace,
                                         size_t workspace_bytes, nvfp4_stream_t stream);
 
+/* Bytes of the MMA-ready layout of the block scales of a [rows][cols] matrix: rows padded to 128
+ * and scale columns (cols/16) padded to 4. */
+size_t nvfp4_swizzled_scales_bytes(int64_t rows, int64_t cols);
+
+/* Re-lays row-major E4M3 block scales [rows][cols/16] into the layout block-scaled tensor-core
+ * GEMMs read: tiles of 128 rows x 4 scale columns (512 bytes), tiles row-major over
+ * [ceil(rows/128)][ceil(cols/64)], the scale of (row r, scale column c) at byte
+ * (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4) of its tile; padding is zero.
+ * swizzled: device buffer of nvfp4_swizzled_scales_bytes(rows, cols) bytes. */
+nvfp4_status nvfp4_swizzle_block_scales(const uint8_t* block_scales, int64_t rows, int64_t cols,
+                                        uint8_t* swizzled, nvfp4_stream_t stream);
+
+/* Device workspace nvfp4_gemm_nt needs for an m x n product (library GEMM scratch plus the FP32
+ * accumulator). */
+size_t nvfp4_gemm_workspace_bytes(int64_t m, int64_t n);
+
+/* The forward the quantized tensors feed ("NVFP4 RL" Sec. 3: y = x . Q(w); Sec. 2: x with per-token
+ * FP32 scales): y[m][n] = bf16(fp32(fp32(D[m][n] * x_row_scale[m]) * w_tensor_scale[0])) with
+ * D[m][n] = sum_k (qx[m][k] * sx[m][k/16]) * (qw[n][k] * sw[n][k/16]) accumulated in FP32 on the
+ * tensor cores (NVFP4 x NVFP4 block-scaled product, the library's GEMM), then one epilogue pass.
+ *   x_codes [m][k/2], w_codes [n][k/2]   E2M1 codes as the quantizer writes them (256-byte aligned)
+ *   x_scales_swizzled, w_scales_swizzled block scales in the layout of nvfp4_swizzle_block_scales
+ *   x_row_scale [m], w_tensor_scale [1]  the quantizer's S_dec values
+ *   y [m][n] BF16 (16-byte aligned); workspace >= nvfp4_gemm_workspace_bytes(m, n), 256-aligned.
+ * k must be a positive multiple of 64 and n of 16.  Not bit-reproducible across libraries: the
+ * FP32 accumulation order is the library's. */
+nvfp4_status nvfp4_gemm_nt(const uint8_t* x_codes, const uint8_t* x_scales_swizzled,
+                           const float* x_row_scale, const uint8_t* w_codes,
+                           const uint8_t* w_scales_swizzled, const float* w_tensor_scale, int64_t m,
+                           int64_t n, int64_t k, void* y, void* workspace, size_t workspace_bytes,
+                           nvfp4_stream_t stream);
+
 /* Reads (and, if clear != 0, resets to NVFP4_OK) the device status word of the current device.
  * Synchronizes the device.  *status_out receives NVFP4_OK or the first device-side error. */
 nvfp4_status nvfp4_get_device_status(int clear, nvfp4_status* status_out);

@@ -19,7 +19,8 @@ __all__ = [
     "Nvfp4Error", "MODE_SIX", "MODE_FOUR_OVER_SIX", "SCALE_ROW", "SCALE_TENSOR",
     "nvfp4_quantize_rowwise", "nvfp4_quantize_residual", "nvfp4_row_amax", "nvfp4_quantize_guided", "nvfp4_quantize_tensor", "nvfp4_quantize_tensor_with_amax",
     "nvfp4_tensor_amax", "nvfp4_quantize_tensor_noalloc", "nvfp4_dequantize", "nvfp4_fused_roundtrip",
-    "nvfp4_tensor_workspace_bytes", "nvfp4_get_device_status", "nvfp4_status_string",
+    "nvfp4_swizzled_scales_bytes", "nvfp4_swizzle_block_scales", "nvfp4_gemm_workspace_bytes",
+    "nvfp4_gemm_nt", "nvfp4_tensor_workspace_bytes", "nvfp4_get_device_status", "nvfp4_status_string",
     "nvfp4_set_launch_config", "nvfp4_selftest_wait_timeout", "nvfp4_abi_version", "library",
 ]
 
@@ -72,6 +73,10 @@ def library():
         "nvfp4_quantize_tensor_noalloc": [P, I64, I64, I, P, P, P, P],
         "nvfp4_quantize_residual": [P, I64, I64, I, P, P, P, P, P, P, P],
         "nvfp4_row_amax": [P, I64, I64, P, P],
+        "nvfp4_swizzled_scales_bytes": [I64, I64],
+        "nvfp4_swizzle_block_scales": [P, I64, I64, P, P],
+        "nvfp4_gemm_workspace_bytes": [I64, I64],
+        "nvfp4_gemm_nt": [P, P, P, P, P, P, I64, I64, I64, P, P, SZ, P],
         "nvfp4_quantize_guided": [P, I64, I64, I, P, P, P, P, P],
         "nvfp4_dequantize": [P, P, P, I, I64, I64, P, P],
         "nvfp4_fused_roundtrip": [P, I64, I64, I, I, P, P, P, P, P, SZ, P],
@@ -89,6 +94,8 @@ def library():
         fn.restype = I
     lib.nvfp4_tensor_workspace_bytes.restype = SZ
     lib.nvfp4_roundtrip_host_workspace_bytes.restype = SZ
+    lib.nvfp4_swizzled_scales_bytes.restype = SZ
+    lib.nvfp4_gemm_workspace_bytes.restype = SZ
     lib.nvfp4_status_string.restype = ctypes.c_char_p
     _lib = lib
     return lib
@@ -191,6 +198,45 @@ def nvfp4_quantize_guided(x, row_amax, ref_codes, ref_block_scales, mode="four_o
                                          _stream(stream, dev))
     _check(st, "nvfp4_quantize_guided")
     return codes
+
+
+def nvfp4_swizzled_scales_bytes(rows, cols):
+    return int(library().nvfp4_swizzled_scales_bytes(int(rows), int(cols)))
+
+
+def nvfp4_swizzle_block_scales(block_scales, cols, out=None, stream=None):
+    """Row-major E4M3 block scales [rows, cols/16] -> the MMA-ready tiled layout (uint8, 1-D)."""
+    rows = block_scales.shape[0]
+    dev = block_scales.device
+    _need(block_scales, "block_scales", torch.uint8, (rows, cols // 16), dev)
+    n = nvfp4_swizzled_scales_bytes(rows, cols)
+    out = _out(out, "out", torch.uint8, (n,), dev)
+    _check(library().nvfp4_swizzle_block_scales(_ptr(block_scales), rows, cols, _ptr(out),
+                                                _stream(stream, dev)),
+           "nvfp4_swizzle_block_scales")
+    return out
+
+
+def nvfp4_gemm_workspace_bytes(m, n):
+    return int(library().nvfp4_gemm_workspace_bytes(int(m), int(n)))
+
+
+def nvfp4_gemm_nt(x_codes, x_scales_swizzled, x_row_scale, w_codes, w_scales_swizzled,
+                  w_tensor_scale, y=None, workspace=None, stream=None):
+    """y[m, n] = x . w^T from NVFP4 operands (per-token x scale, per-tensor w scale), BF16."""
+    m, k = x_codes.shape[0], x_codes.shape[1] * 2
+    n = w_codes.shape[0]
+    dev = x_codes.device
+    y = _out(y, "y", torch.bfloat16, (m, n), dev)
+    need = nvfp4_gemm_workspace_bytes(m, n)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    st = library().nvfp4_gemm_nt(_ptr(x_codes), _ptr(x_scales_swizzled), _ptr(x_row_scale),
+                                 _ptr(w_codes), _ptr(w_scales_swizzled), _ptr(w_tensor_scale),
+                                 m, n, k, _ptr(y), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream, dev))
+    _check(st, "nvfp4_gemm_nt")
+    return y
 
 
 def nvfp4_tensor_workspace_bytes():

@@ -16,7 +16,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIBRARY = os.path.join(LIBDIR, "libnvfp4_gb300.so")
-SOURCES = ["nvfp4_quant.cu", "nvfp4_aux.cu", "nvfp4_capi.cu", "nvfp4_noalloc.cu", "nvfp4_host.cu"]
+SOURCES = ["nvfp4_quant.cu", "nvfp4_aux.cu", "nvfp4_capi.cu", "nvfp4_noalloc.cu", "nvfp4_host.cu",
+           "nvfp4_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC]
@@ -61,7 +62,9 @@ def build(force=False, verbose=False, extra=()):
         logs = list(ex.map(run, cmds))
     objs = [c[-1] for c in cmds]
     tmp = LIBRARY + ".tmp"
-    link = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+    cuda_lib = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
+    link = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-L", cuda_lib, "-lcublasLt",
+            "-Xlinker", "-rpath=" + cuda_lib]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + " ".join(link) + "\n" + r.stdout + r.stderr)

@@ -402,3 +402,52 @@ def test_fp16_selector_edge_values():
     x = _edge_matrix(37, 7184, seed=11)
     check_rowwise(x, F16)
     check_tensor(x[:9].contiguous(), F16)
+
+
+
+def _swizzle_reference(scales):
+    """The tiled layout written out plainly: tile (r // 128, c // 4), byte
+    (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4 inside it, zero padding."""
+    rows, sc = scales.shape
+    tr, tc = -(-rows // 128), -(-sc // 4)
+    out = np.zeros(tr * tc * 512, np.uint8)
+    for r in range(rows):
+        for c in range(sc):
+            tile = (r // 128) * tc + c // 4
+            out[tile * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4] = scales[r, c]
+    return out
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (130, 7168), (256, 2048), (77, 1040)])
+def test_swizzle_block_scales(rows, cols):
+    x = _edge_matrix(rows, cols, seed=rows)
+    _, scales, _ = nv.nvfp4_quantize_rowwise(x)
+    got = nv.nvfp4_swizzle_block_scales(scales, cols)
+    assert np.array_equal(_np(got), _swizzle_reference(_np(scales)))
+
+
+@pytest.mark.parametrize("m,n,k", [(256, 256, 2048), (512, 384, 7168)])
+def test_gemm_nt_matches_float64_product(m, n, k):
+    """y = x . Q(w) on the tensor cores against the float64 product of the exactly dequantized
+    operands (decoded independently of the library), within FP32-accumulation error."""
+    from indep import exact_dequant
+
+    x = synth.generate(2, device=DEV, rows=m)["x"][:, :k].contiguous()
+    w = synth.generate(1, device=DEV, rows=n)["x"][:, :k].contiguous()
+    xc, xs, xd = nv.nvfp4_quantize_rowwise(x)
+    wc, ws, wd = nv.nvfp4_quantize_tensor(w)
+    y = nv.nvfp4_gemm_nt(xc, nv.nvfp4_swizzle_block_scales(xs, k), xd,
+                         wc, nv.nvfp4_swizzle_block_scales(ws, k), wd)
+    X = exact_dequant({"codes": _np(xc), "scales": _np(xs), "scale": _np(xd)}, k)
+    W = exact_dequant({"codes": _np(wc), "scales": _np(ws), "scale": _np(wd)}, k)
+    ref = X @ W.T
+    mag = np.abs(X) @ np.abs(W).T
+    got = y.float().cpu().numpy().astype(np.float64)
+    # BF16 output rounding (2^-9, plus the two FP32 epilogue roundings) and FP32 accumulation over
+    # k terms (at most k * 2^-24 of the magnitude sum; 7168 * 2^-24 = 4.3e-4).
+    bound = 2.0 ** -8 * np.abs(ref) + k * 2.0 ** -24 * mag + 1e-30
+    print(f"gemm {m}x{n}x{k}: max |err| / (|ref| + k 2^-24 mag) = "
+          f"{(np.abs(got - ref) / (np.abs(ref) + k * 2.0 ** -24 * mag + 1e-30)).max():.3e}")
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), f"{bad.sum()} of {bad.size} outputs off; worst {np.abs(got - ref)[bad].max()}"
+    assert nv.nvfp4_get_device_status() == 0
