@@ -139,3 +139,36 @@ def test_factors_zero_and_tiny_amax():
     assert 0 < S_dec < np.finfo(np.float32).tiny
     S_enc, c6, c4, _ = oracle.factors(np.float32(2.0 ** -126), oracle.MODE_FOUR_OVER_SIX)
     assert S_enc == c6 == c4 == np.finfo(np.float32).max
+
+
+def _f32_nearest(q):
+    """Correctly rounded float32 of an exact rational (ties to even), by comparing the two float32
+    neighbours of the float64 approximation in exact arithmetic."""
+    from fractions import Fraction
+
+    x = np.float32(float(q))
+    lo, hi = (x, np.nextafter(x, np.float32(np.inf))) if Fraction(float(x)) <= q else \
+             (np.nextafter(x, np.float32(-np.inf)), x)
+    dl, dh = q - Fraction(float(lo)), Fraction(float(hi)) - q
+    if dl < dh:
+        return lo
+    if dh < dl:
+        return hi
+    return lo if (lo.view(np.uint32) & 1) == 0 else hi
+
+
+@pytest.mark.parametrize("mode,M", [(oracle.MODE_FOUR_OVER_SIX, 256), (oracle.MODE_SIX, 448)])
+def test_factors_are_correctly_rounded_quotients(mode, M):
+    """S_enc = 6M/a, c6 = M/a, c4 = 1.5M/a and S_dec = a/(6M), each the correctly rounded FP32
+    value of the exact quotient (the candidate formula's amax / (E2M1_MAXVAL * M))."""
+    from fractions import Fraction
+
+    rng = np.random.default_rng(21)
+    amaxes = (rng.standard_normal(400) * np.exp(rng.uniform(-30, 30, 400))).astype(np.float32)
+    for a in np.abs(amaxes[amaxes != 0]):
+        fa = Fraction(float(a))
+        S_enc, c6, c4, S_dec = oracle.factors(a, mode)
+        assert S_enc == _f32_nearest(Fraction(6 * M) / fa)
+        assert c6 == _f32_nearest(Fraction(M) / fa)
+        assert c4 == _f32_nearest(Fraction(3 * M, 2) / fa)
+        assert S_dec == _f32_nearest(fa / (6 * M))
