@@ -8,7 +8,8 @@ the device (seeded) and stay resident; the 235 MB input exceeds the 129 MB L2, s
 the previous step's data from L2.
 
   value     algorithmic HBM bytes (2 B in + 0.5625 B codes/scales + 2 B y per element + 4 B per
-            row) per step / device time per step, summed over ranks, in GB/s
+            row) per step / device time per step, summed over ranks, in GB/s; the K timed steps
+            are captured once into a CUDA graph and replayed (no host launch overhead)
   e2e       the same metric through the public API with pinned host buffers: every step copies
             x host->device, runs the call, and copies all outputs back
   roofline  the fused kernel's achieved GB/s against the measured HBM copy bandwidth
@@ -161,15 +162,37 @@ def max_over_ranks(value, world, device):
     return float(t.item())
 
 
-def time_steps(fn, steps, warmup, world, device):
-    """W warm-up calls, then K timed calls bracketed by barrier + synchronize.  Returns
-    (per-step device ms list, whole-region ms)."""
+def time_steps(fn, steps, warmup, world, device, graph=True):
+    """W warm-up calls, then K timed calls bracketed by barrier + synchronize.  With `graph` the K
+    calls are captured once into a CUDA graph and the timed region is one replay of it (host
+    launch overhead out of the way, as in a captured training step); per-step times are then the
+    replay time / K.  Returns (per-step device ms list, whole-region ms)."""
     stream = torch.cuda.current_stream(device)
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize(device)
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(steps):
+                fn()
+        torch.cuda.synchronize(device)
+        g.replay()  # one untimed replay
+        torch.cuda.synchronize(device)
     barrier(world)
     torch.cuda.synchronize(device)
+    if graph:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        torch.cuda.synchronize(device)
+        region = start.elapsed_time(end)
+        return [region / steps] * steps, region
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
@@ -406,6 +429,7 @@ def main():
                    "rows": rows, "cols": cols, "op": "fused quantize->dequantize round trip",
                    "scale": "row (per-token)", "mode": "four_over_six",
                    "l2": f"inputs larger than L2 ({rows * cols * 2 / 1e6:.0f} MB > 129 MB), no flush",
+                   "timing": "K steps captured in one CUDA graph, one replay timed with CUDA events",
                    "parallelism": f"replicas x{world}"},
         "elem_per_s": round(world * rows * cols / (ms * 1e-3), 1),
         "frac_of_hbm_peak": round(achieved / peak, 4),

@@ -67,6 +67,9 @@ constexpr int kAmaxUnroll = 4;
 // Partial max |x| per CTA over a grid-strided range of 16-byte vectors, plus the scalar tail.
 __global__ void __launch_bounds__(kAmaxThreads) amax_partials_kernel(const uint16_t* x, int64_t n,
                                                                      float* partials) {
+  // The encoder that consumes the partials may start its own prologue (and its reads of x, which
+  // this kernel does not write) right away; it waits for this grid before reading the partials.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t nvec = n / 8;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kAmaxThreads;

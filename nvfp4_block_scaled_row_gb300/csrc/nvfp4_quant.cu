@@ -265,16 +265,6 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
   const uint64_t policy = l2_evict_first_policy();
   const int h0 = (lane >> 2) & 1;  // which 16-byte half of its block this lane reads first
 
-  RowFactors f{};
-  if (kTensor) {
-    float a = 0.0f;
-    for (int i = lane; i < p.n_amax; i += 32) a = fmaxf(a, p.amax_src[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-    f = row_factors<kMode>(a);
-    if (blockIdx.x == 0 && threadIdx.x == 0) p.scale_out[0] = f.S_dec;
-  }
-
   // Prologue: fill the ring with this warp's part of the team's first rows.
   int64_t issued = 0;
   auto issue = [&](int slot_index, int64_t row) {
@@ -285,6 +275,19 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
   };
   if (lane == 0 && has_work)
     for (int s = 0; s < S && gt + s * NT < p.rows; ++s) issue(s, gt + s * NT);
+
+  RowFactors f{};
+  if (kTensor) {
+    // Tensor scale: this grid may be a programmatic dependent of the amax kernel (x is not written
+    // there, so the copies above may already run); the partial maxima need that grid complete.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    float a = 0.0f;
+    for (int i = lane; i < p.n_amax; i += 32) a = fmaxf(a, p.amax_src[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+    f = row_factors<kMode>(a);
+    if (blockIdx.x == 0 && threadIdx.x == 0) p.scale_out[0] = f.S_dec;
+  }
 
   int64_t k = 0;
   for (int64_t row = gt; row < p.rows; row += NT, ++k) {
@@ -610,8 +613,22 @@ cudaError_t launch_impl(QuantParams p, cudaStream_t stream) {
   p.team = rs.team;
   p.blocks_per_warp = rs.blocks_per_warp;
   p.slot_bytes = rs.slot_bytes;
-  kern<<<static_cast<unsigned>(grid), rs.warps * 32, rs.smem, stream>>>(p);
-  return cudaGetLastError();
+  if (!kTensor) {
+    kern<<<static_cast<unsigned>(grid), rs.warps * 32, rs.smem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  // Tensor scale: launched as a programmatic dependent of the preceding amax kernel.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(rs.warps * 32);
+  cfg.dynamicSmemBytes = rs.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
