@@ -128,7 +128,7 @@ nvfp4_status run_tensor(const void* x, int64_t rows, int64_t cols, int mode, uin
   QuantParams p = base_params(x, rows, cols, codes, block_scales, scale, y, status);
   p.amax_src = partials;
   p.n_amax = n_partials;
-  return from_cuda(launch_quantize(mode, true, fused, p, stream));
+  return from_cuda(launch_quantize(mode, true, fused, p, stream, true));
 }
 
 }  // namespace

@@ -22,8 +22,10 @@ int sm_count(int device);
 
 // Quantize: row scale (kTensor = false) or tensor scale, plain or fused round trip.
 // Chooses the ring shape from cols; returns cudaErrorInvalidValue when cols cannot be staged.
+// after_amax_kernel: a tensor-scale launch that directly follows launch_amax_partials* on the
+// same stream (p.amax_src = its partials) starts as that kernel's programmatic dependent.
 cudaError_t launch_quantize(int mode, bool tensor_scale, bool fused, QuantParams p,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool after_amax_kernel = false);
 
 // Row-scale quantization of x and of its BF16 residual x - DQ(Q(x)) in one pass over x
 // (p.res_codes, p.res_scales, p.res_scale_out receive the residual's outputs).

@@ -86,6 +86,6 @@ extern "C" nvfp4_status nvfp4_quantize_tensor_noalloc(const void* x, int64_t row
   p.n_amax = n_partials;
   p.status = status;
   p.timeout_ns = 4000000000ull;
-  return nvfp4::launch_quantize(mode, true, false, p, s) == cudaSuccess ? NVFP4_OK
-                                                                        : NVFP4_ERR_CUDA;
+  return nvfp4::launch_quantize(mode, true, false, p, s, true) == cudaSuccess ? NVFP4_OK
+                                                                              : NVFP4_ERR_CUDA;
 }

@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
   if (kTensor) {
     // Tensor scale: this grid may be a programmatic dependent of the amax kernel (x is not written
     // there, so the copies above may already run); the partial maxima need that grid complete.
+    // Launched the ordinary way, the wait returns at once.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     float a = 0.0f;
     for (int i = lane; i < p.n_amax; i += 32) a = fmaxf(a, p.amax_src[i]);
@@ -564,7 +565,7 @@ struct LaunchCache {
 };
 
 template <int kMode, bool kTensor, bool kFused, bool kResidual>
-cudaError_t launch_impl(QuantParams p, cudaStream_t stream) {
+cudaError_t launch_impl(QuantParams p, cudaStream_t stream, bool after_amax_kernel = false) {
   static LaunchCache cache;
   RingShape rs;
   if (!choose_ring(p.cols, &rs)) return cudaErrorInvalidValue;
@@ -613,11 +614,14 @@ cudaError_t launch_impl(QuantParams p, cudaStream_t stream) {
   p.team = rs.team;
   p.blocks_per_warp = rs.blocks_per_warp;
   p.slot_bytes = rs.slot_bytes;
-  if (!kTensor) {
+  if (!kTensor || !after_amax_kernel) {
     kern<<<static_cast<unsigned>(grid), rs.warps * 32, rs.smem, stream>>>(p);
     return cudaGetLastError();
   }
-  // Tensor scale: launched as a programmatic dependent of the preceding amax kernel.
+  // Tensor scale right after our amax kernel: launched as its programmatic dependent.  Only then,
+  // because the row copies issued before griddepcontrol.wait are safe only while the grid this
+  // one depends on does not write x (the amax kernel only reads it, and it started after
+  // everything before it on the stream had finished).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(rs.warps * 32);
@@ -639,21 +643,23 @@ bool quantize_cols_supported(int64_t cols) {
 }
 
 template <int kMode>
-cudaError_t launch_mode(bool tensor_scale, bool fused, QuantParams p, cudaStream_t stream) {
+cudaError_t launch_mode(bool tensor_scale, bool fused, QuantParams p, cudaStream_t stream,
+                        bool after_amax_kernel) {
   if (tensor_scale)
-    return fused ? launch_impl<kMode, true, true, false>(p, stream)
-                 : launch_impl<kMode, true, false, false>(p, stream);
+    return fused ? launch_impl<kMode, true, true, false>(p, stream, after_amax_kernel)
+                 : launch_impl<kMode, true, false, false>(p, stream, after_amax_kernel);
   return fused ? launch_impl<kMode, false, true, false>(p, stream)
                : launch_impl<kMode, false, false, false>(p, stream);
 }
 
 cudaError_t launch_quantize(int mode, bool tensor_scale, bool fused, QuantParams p,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool after_amax_kernel) {
   switch (mode) {
-    case kModeFourOverSix: return launch_mode<kModeFourOverSix>(tensor_scale, fused, p, stream);
+    case kModeFourOverSix:
+      return launch_mode<kModeFourOverSix>(tensor_scale, fused, p, stream, after_amax_kernel);
     case kModeFourOverSixFp16:
-      return launch_mode<kModeFourOverSixFp16>(tensor_scale, fused, p, stream);
-    default: return launch_mode<kModeSix>(tensor_scale, fused, p, stream);
+      return launch_mode<kModeFourOverSixFp16>(tensor_scale, fused, p, stream, after_amax_kernel);
+    default: return launch_mode<kModeSix>(tensor_scale, fused, p, stream, after_amax_kernel);
   }
 }
 
