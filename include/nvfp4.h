@@ -191,7 +191,7 @@ nvfp4_status nvfp4_fused_roundtrip(const void* x, int64_t rows, int64_t cols,
                                    size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* Bytes of device staging workspace nvfp4_fused_roundtrip_host needs for rows of `cols`
- * elements (three chunk buffers of ~16 MB of input each); 0 for an invalid cols. */
+ * elements (three chunk buffers of ~32 MB of input each); 0 for an invalid cols. */
 size_t nvfp4_roundtrip_host_workspace_bytes(int64_t cols);
 
 /* nvfp4_fused_roundtrip with the row scale for a matrix in HOST memory ("NVFP4 RL" Sec. 6: the

@@ -8,9 +8,12 @@
 // direction and the SMs, so host->device copies, kernels and device->host copies overlap.  Events
 // order the internal streams after everything already queued on the caller's stream, and the
 // caller's stream after all of them, so the call behaves like any other asynchronous call on
-// `stream`.
+// `stream`.  The internal streams and events are created once per device and kept; one host
+// thread at a time queues work on them (a per-device mutex), so concurrent callers stay ordered
+// after their own streams.
 // Per-token results do not depend on chunking, so the outputs equal nvfp4_fused_roundtrip's.
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "nvfp4.h"
@@ -18,7 +21,7 @@
 
 namespace {
 
-constexpr int64_t kChunkBytesTarget = 16ll << 20;  // ~16 MB of input per chunk
+constexpr int64_t kChunkBytesTarget = 32ll << 20;  // ~32 MB of input per chunk
 constexpr int kStages = 3;                          // chunk buffers / internal streams
 
 struct ChunkLayout {
@@ -27,6 +30,40 @@ struct ChunkLayout {
 };
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// The per-device internal streams and events (created on first use, kept for the process).
+struct Pipe {
+  bool ready = false;
+  cudaStream_t s[kStages] = {};
+  cudaEvent_t start = nullptr;
+  cudaEvent_t done[kStages] = {};
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_pipe_mutex[kMaxDevices];
+Pipe g_pipe[kMaxDevices];
+
+// Creates the device's pipe if needed; the caller holds g_pipe_mutex[device].
+cudaError_t ensure_pipe(Pipe& p) {
+  if (p.ready) return cudaSuccess;
+  cudaError_t e = cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming);
+  for (int i = 0; i < kStages && e == cudaSuccess; ++i) {
+    e = cudaStreamCreateWithFlags(&p.s[i], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.done[i], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) {  // leave nothing half made
+    for (int i = 0; i < kStages; ++i) {
+      if (p.s[i] != nullptr) cudaStreamDestroy(p.s[i]);
+      if (p.done[i] != nullptr) cudaEventDestroy(p.done[i]);
+      p.s[i] = nullptr;
+      p.done[i] = nullptr;
+    }
+    if (p.start != nullptr) cudaEventDestroy(p.start);
+    p.start = nullptr;
+    return e;
+  }
+  p.ready = true;
+  return cudaSuccess;
+}
 
 ChunkLayout layout_for(int64_t cols) {
   ChunkLayout L;
@@ -71,27 +108,26 @@ extern "C" nvfp4_status nvfp4_fused_roundtrip_host(const void* x, int64_t rows, 
 
   int* status = nullptr;
   if (nvfp4::device_status_word(&status) != cudaSuccess) return NVFP4_ERR_CUDA;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+    return NVFP4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_pipe_mutex[device]);
+  Pipe& pipe = g_pipe[device];
+  if (ensure_pipe(pipe) != cudaSuccess) return NVFP4_ERR_CUDA;
   cudaStream_t caller = reinterpret_cast<cudaStream_t>(stream);
-  cudaStream_t s[kStages] = {};
-  cudaEvent_t start = nullptr, done[kStages] = {};
   nvfp4_status result = NVFP4_OK;
   auto check = [&](cudaError_t e) {
     if (e != cudaSuccess && result == NVFP4_OK) result = NVFP4_ERR_CUDA;
     return e == cudaSuccess;
   };
-  if (!check(cudaEventCreateWithFlags(&start, cudaEventDisableTiming))) goto cleanup;
+  if (!check(cudaEventRecord(pipe.start, caller))) return result;
   for (int i = 0; i < kStages; ++i)
-    if (!check(cudaStreamCreateWithFlags(&s[i], cudaStreamNonBlocking)) ||
-        !check(cudaEventCreateWithFlags(&done[i], cudaEventDisableTiming)))
-      goto cleanup;
-  if (!check(cudaEventRecord(start, caller))) goto cleanup;
-  for (int i = 0; i < kStages; ++i)
-    if (!check(cudaStreamWaitEvent(s[i], start, 0))) goto cleanup;
+    if (!check(cudaStreamWaitEvent(pipe.s[i], pipe.start, 0))) return result;
 
   for (int64_t r0 = 0, c = 0; r0 < rows; r0 += L.rows, ++c) {
     const int64_t n = (rows - r0 < L.rows) ? rows - r0 : L.rows;
     const int h = static_cast<int>(c % kStages);
-    cudaStream_t st = s[h];
+    cudaStream_t st = pipe.s[h];
     unsigned char* base = static_cast<unsigned char*>(workspace) + h * L.total;
     const size_t xb = static_cast<size_t>(n * cols * 2);
     const size_t cb = static_cast<size_t>(n * cols / 2);
@@ -122,15 +158,7 @@ extern "C" nvfp4_status nvfp4_fused_roundtrip_host(const void* x, int64_t rows, 
   }
   // Whatever was queued, the caller's stream waits for all of it.
   for (int i = 0; i < kStages; ++i)
-    if (check(cudaEventRecord(done[i], s[i]))) check(cudaStreamWaitEvent(caller, done[i], 0));
-
-cleanup:
-  // Destroying streams and events with work pending is allowed: they are released once it ends.
-  // (An early failure can leave the caller's stream without a wait: nothing was queued then.)
-  for (cudaStream_t st : s)
-    if (st != nullptr) cudaStreamDestroy(st);
-  if (start != nullptr) cudaEventDestroy(start);
-  for (cudaEvent_t e : done)
-    if (e != nullptr) cudaEventDestroy(e);
+    if (check(cudaEventRecord(pipe.done[i], pipe.s[i])))
+      check(cudaStreamWaitEvent(caller, pipe.done[i], 0));
   return result;
 }
