@@ -423,6 +423,22 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
   }
 }
 
+// Sign masks of eight FP32 values as nibbles: nibble i of the result is 0xF when v[i] has its
+// sign bit set, else 0.  prmt's sign-replicating selectors (selector msb set) copy the top bit of
+// byte 3 of each value into a whole byte; two bytes per element pair are then merged into nibbles.
+__device__ __forceinline__ uint32_t sign_nibbles(const float (&v)[8]) {
+  uint32_t a, b, even, p02, p46, p13, p57, odd;
+  asm("prmt.b32 %0, %1, %2, 0x00FB;" : "=r"(p02) : "f"(v[0]), "f"(v[2]));
+  asm("prmt.b32 %0, %1, %2, 0xFB00;" : "=r"(p46) : "f"(v[4]), "f"(v[6]));
+  asm("prmt.b32 %0, %1, %2, 0x7610;" : "=r"(a) : "r"(p02), "r"(p46));
+  asm("prmt.b32 %0, %1, %2, 0x00FB;" : "=r"(p13) : "f"(v[1]), "f"(v[3]));
+  asm("prmt.b32 %0, %1, %2, 0xFB00;" : "=r"(p57) : "f"(v[5]), "f"(v[7]));
+  asm("prmt.b32 %0, %1, %2, 0x7610;" : "=r"(b) : "r"(p13), "r"(p57));
+  even = a & 0x0F0F0F0Fu;  // byte k: element 2k -> low nibble
+  odd = b & 0xF0F0F0F0u;   // byte k: element 2k+1 -> high nibble
+  return even | odd;
+}
+
 // TRACE rollout-guided rounding ("TRACE FP4 RL -- Rollout-guided FP4 rounding"): with the
 // rollout's per-token amax and block scales, each element's scaled value t is formed exactly as
 // the quantizer forms it; of its two neighbouring codewords the one closer to the rollout's
@@ -431,6 +447,13 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
 // rounding went away from zero they are (m-1, m), towards zero (m, m+1), none if t is on the grid
 // or saturated.  Of two adjacent magnitudes the larger is closer to the rollout's codeword exactly
 // when that codeword lies on t's side of zero with magnitude >= it.
+//
+// The decision runs on all eight nibbles of a code word at once.  With u = r - t and v = t - r
+// (both exact in sign; both +0 when t is on the grid), rounding went away from zero where
+// t >= 0 and v < 0, or t < 0 and u < 0; towards zero where t >= 0 and u < 0, or t < 0 and v < 0.
+// Magnitude comparisons of the rollout's codes R with m use borrow-free nibble subtraction
+// ((R | 8) - m keeps bit 3 exactly when R >= m).  The magnitude then moves by -1 (away, unless the
+// rollout's code is on the same side with R >= m) or +1 (towards, when it is with R > m).
 template <int kMode>
 __global__ void __launch_bounds__(256) guided_kernel(const GuidedParams p) {
   __shared__ ScaleEntry tab[256];
@@ -441,7 +464,8 @@ __global__ void __launch_bounds__(256) guided_kernel(const GuidedParams p) {
   const int64_t NW = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int cols = p.cols;
   const int ngroups = cols / 8;
-  const uint16_t one_h = 0x3C00;  // FP16 1.0
+  const uint32_t one_h2 = 0x3C003C00u;   // FP16 (1, 1)
+  const uint32_t mone_h2 = 0xBC00BC00u;  // FP16 (-1, -1)
   for (int64_t row = gw; row < p.rows; row += NW) {
     const RowFactors f = row_factors_warp<kMode>(p.row_amax[row], lane);
     const f32x2 senc2 = pack2(f.S_enc, f.S_enc);
@@ -454,35 +478,37 @@ __global__ void __launch_bounds__(256) guided_kernel(const GuidedParams p) {
       const uint32_t ref = rr[g];
       const ScaleEntry e = tab[sr[g >> 1]];
       const f32x2 inv2 = pack2(e.inv, e.inv);
-      f32x2 t[4];
-      t[0] = mul2(mul2(bf16x2_to_f32x2(xw.x), senc2), inv2);
-      t[1] = mul2(mul2(bf16x2_to_f32x2(xw.y), senc2), inv2);
-      t[2] = mul2(mul2(bf16x2_to_f32x2(xw.z), senc2), inv2);
-      t[3] = mul2(mul2(bf16x2_to_f32x2(xw.w), senc2), inv2);
+      const f32x2 ninv2 = pack2(-e.inv, -e.inv);
+      f32x2 z[4], t[4];
+      z[0] = mul2(bf16x2_to_f32x2(xw.x), senc2);
+      z[1] = mul2(bf16x2_to_f32x2(xw.y), senc2);
+      z[2] = mul2(bf16x2_to_f32x2(xw.z), senc2);
+      z[3] = mul2(bf16x2_to_f32x2(xw.w), senc2);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) t[j] = mul2(z[j], inv2);
       uint32_t r[4];
       const uint32_t rtn = e2m1x8_encode_decode(t[0], t[1], t[2], t[3], r);
-      // d = r - t per element (r exact in FP16, one rounding); its sign says which way t went.
-      float tv[8], dv[8];
+      float u[8], v[8];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        unpack2(t[j], tv[2 * j], tv[2 * j + 1]);
-        const f32x2 dd = fma_f16x2_f32x2(r[j], one_h | (one_h << 16), pack2(-tv[2 * j], -tv[2 * j + 1]));
-        unpack2(dd, dv[2 * j], dv[2 * j + 1]);
+        const f32x2 nt = mul2(z[j], ninv2);                     // -t, exactly
+        const f32x2 uj = fma_f16x2_f32x2(r[j], one_h2, nt);     // r - t, one rounding
+        const f32x2 vj = fma_f16x2_f32x2(r[j], mone_h2, t[j]);  // t - r, one rounding
+        unpack2(uj, u[2 * j], u[2 * j + 1]);
+        unpack2(vj, v[2 * j], v[2 * j + 1]);
       }
-      uint32_t word = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float ti = tv[i], d = dv[i];
-        const uint32_t code = (rtn >> (4 * i)) & 0xFu;
-        const uint32_t m = code & 7u, sign = code >> 3;
-        const bool away = (d > 0.0f && ti > 0.0f) || (d < 0.0f && ti < 0.0f);
-        const uint32_t m_lo = away ? m - 1 : m;
-        const uint32_t m_hi = (d == 0.0f || away) ? m : min(m + 1, 7u);
-        const uint32_t rc = (ref >> (4 * i)) & 0xFu;
-        const bool take_hi = m_hi != m_lo && (rc >> 3) == sign && (rc & 7u) >= m_hi;
-        word |= ((sign << 3) | (take_hi ? m_hi : m_lo)) << (4 * i);
-      }
-      out[g] = word;
+      const uint32_t su = sign_nibbles(u), sv = sign_nibbles(v);
+      const uint32_t st = rtn & 0x88888888u;                        // sign of t (bit 3)
+      const uint32_t away = (st & su) | (~st & sv);                 // bit 3 meaningful
+      const uint32_t toward = (st & sv) | (~st & su);
+      const uint32_t mag = rtn & 0x77777777u;
+      const uint32_t rg = ref | 0x88888888u;
+      const uint32_t ge = rg - mag;                                 // bit 3: R >= m
+      const uint32_t gt = rg - mag - 0x11111111u;                   // bit 3: R > m
+      const uint32_t other = rtn ^ ref;                             // bit 3: R on the other side
+      const uint32_t down = away & (~ge | other) & 0x88888888u;
+      const uint32_t up = toward & gt & ~other & 0x88888888u;
+      out[g] = rtn + (up >> 3) - (down >> 3);
     }
   }
 }
