@@ -302,7 +302,7 @@ def test_sharded_tensor_helper_on_one_rank():
 def test_host_streamed_roundtrip_matches_device_call():
     """Host-resident input streamed in chunks (several chunks and a ragged last one) gives the
     device call's outputs exactly, for both modes."""
-    x = synth.generate(2, device=DEV, rows=2500)["x"]
+    x = synth.generate(2, device=DEV, rows=5000)["x"]  # three ~32 MB chunks, the last ragged
     xh = x.cpu().pin_memory()
     for mode in (F4, SIX):
         want = nv.nvfp4_fused_roundtrip(x, "row", mode)
@@ -315,6 +315,55 @@ def test_host_streamed_roundtrip_matches_device_call():
     torch.cuda.current_stream().synchronize()
     assert torch.equal(got[0], nv.nvfp4_fused_roundtrip(x[:300].contiguous())[0].cpu())
     assert nv.nvfp4_get_device_status() == 0
+
+
+def test_host_streamed_roundtrip_concurrent_callers():
+    """Two host threads streaming different matrices on their own streams at the same time (the
+    internal streams are shared per device) each get their own device call's outputs."""
+    import threading
+
+    xs = [synth.generate(i, device=DEV, rows=3000)["x"] for i in (2, 4)]
+    hosts = [x.cpu().pin_memory() for x in xs]
+    wants = [nv.nvfp4_fused_roundtrip(x) for x in xs]
+    torch.cuda.synchronize()
+    results, errors = [None, None], []
+
+    def run(i):
+        try:
+            torch.cuda.set_device(0)
+            st = torch.cuda.Stream()
+            outs = []
+            for _ in range(3):
+                outs = nv.nvfp4_fused_roundtrip_host(hosts[i], stream=st)
+            st.synchronize()
+            results[i] = outs
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in (0, 1)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for want, got in zip(wants, results):
+        for a, b in zip(want, got):
+            assert torch.equal(a.cpu().view(torch.uint8), b.view(torch.uint8))
+    assert nv.nvfp4_get_device_status() == 0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_shapes_against_oracle(seed):
+    """Random widths (any multiple of 16 up to 8192), row counts and modes, row and tensor scale,
+    on the edge-case value mix."""
+    rng = np.random.default_rng(100 + seed)
+    for _ in range(4):
+        cols = 16 * int(rng.integers(1, 513))
+        rows = int(rng.integers(1, 97))
+        mode = (F4, SIX, F16)[int(rng.integers(0, 3))]
+        x = _edge_matrix(rows, cols, seed=int(rng.integers(1 << 30)))
+        check_rowwise(x, mode)
+        check_tensor(x, mode)
 
 
 def check_residual(x, mode=F4, rows_idx=None):
