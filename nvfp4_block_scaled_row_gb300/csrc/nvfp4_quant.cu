@@ -423,6 +423,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
   }
 }
 
+constexpr int kGuidedUnroll = 4;  // 8-element groups per lane per step of the guided encoder
+
 // Sign masks of eight FP32 values as nibbles: nibble i of the result is 0xF when v[i] has its
 // sign bit set, else 0.  prmt's sign-replicating selectors (selector msb set) copy the top bit of
 // byte 3 of each value into a whole byte; two bytes per element pair are then merged into nibbles.
@@ -466,49 +468,81 @@ __global__ void __launch_bounds__(256) guided_kernel(const GuidedParams p) {
   const int ngroups = cols / 8;
   const uint32_t one_h2 = 0x3C003C00u;   // FP16 (1, 1)
   const uint32_t mone_h2 = 0xBC00BC00u;  // FP16 (-1, -1)
-  for (int64_t row = gw; row < p.rows; row += NW) {
-    const RowFactors f = row_factors_warp<kMode>(p.row_amax[row], lane);
-    const f32x2 senc2 = pack2(f.S_enc, f.S_enc);
+  // Work units: kGuidedUnroll * 32 consecutive 8-element groups of one row, so a lane has
+  // kGuidedUnroll independent loads in flight.  Each warp takes a contiguous range of units (the
+  // row factors are recomputed only when the row changes), which balances rows across warps.
+  const int units_per_row = (ngroups + 32 * kGuidedUnroll - 1) / (32 * kGuidedUnroll);
+  const int64_t total = p.rows * units_per_row;
+  const int64_t per_warp = (total + NW - 1) / NW;
+  const int64_t u_begin = gw * per_warp;
+  const int64_t u_end = min(total, u_begin + per_warp);
+  int64_t cur_row = -1;
+  f32x2 senc2 = pack2(0.0f, 0.0f);
+  int64_t row = u_begin / units_per_row;  // walked forward below, without further divisions
+  int unit = static_cast<int>(u_begin - row * units_per_row);
+  for (int64_t u = u_begin; u < u_end; ++u, ++unit) {
+    if (unit == units_per_row) {
+      unit = 0;
+      ++row;
+    }
+    if (row != cur_row) {
+      const RowFactors f = row_factors_warp<kMode>(p.row_amax[row], lane);
+      senc2 = pack2(f.S_enc, f.S_enc);
+      cur_row = row;
+    }
     const uint4* xr = reinterpret_cast<const uint4*>(p.x + row * cols);
     const uint32_t* rr = reinterpret_cast<const uint32_t*>(p.ref_codes + row * (cols / 2));
     const uint8_t* sr = p.ref_scales + row * (cols / kBlockElems);
     uint32_t* out = reinterpret_cast<uint32_t*>(p.codes + row * (cols / 2));
-    for (int g = lane; g < ngroups; g += 32) {
-      const uint4 xw = xr[g];
-      const uint32_t ref = rr[g];
-      const ScaleEntry e = tab[sr[g >> 1]];
+    const int g0 = unit * 32 * kGuidedUnroll + lane;
+    uint4 xw[kGuidedUnroll];
+    uint32_t ref[kGuidedUnroll], sb[kGuidedUnroll];
+#pragma unroll
+    for (int k = 0; k < kGuidedUnroll; ++k) {
+      const int g = g0 + 32 * k;
+      if (g < ngroups) {
+        xw[k] = __ldcs(xr + g);
+        ref[k] = __ldcs(rr + g);
+        sb[k] = sr[g >> 1];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kGuidedUnroll; ++k) {
+      const int g = g0 + 32 * k;
+      if (g >= ngroups) break;
+      const ScaleEntry e = tab[sb[k]];
       const f32x2 inv2 = pack2(e.inv, e.inv);
       const f32x2 ninv2 = pack2(-e.inv, -e.inv);
       f32x2 z[4], t[4];
-      z[0] = mul2(bf16x2_to_f32x2(xw.x), senc2);
-      z[1] = mul2(bf16x2_to_f32x2(xw.y), senc2);
-      z[2] = mul2(bf16x2_to_f32x2(xw.z), senc2);
-      z[3] = mul2(bf16x2_to_f32x2(xw.w), senc2);
+      z[0] = mul2(bf16x2_to_f32x2(xw[k].x), senc2);
+      z[1] = mul2(bf16x2_to_f32x2(xw[k].y), senc2);
+      z[2] = mul2(bf16x2_to_f32x2(xw[k].z), senc2);
+      z[3] = mul2(bf16x2_to_f32x2(xw[k].w), senc2);
 #pragma unroll
       for (int j = 0; j < 4; ++j) t[j] = mul2(z[j], inv2);
       uint32_t r[4];
       const uint32_t rtn = e2m1x8_encode_decode(t[0], t[1], t[2], t[3], r);
-      float u[8], v[8];
+      float uu[8], vv[8];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const f32x2 nt = mul2(z[j], ninv2);                     // -t, exactly
         const f32x2 uj = fma_f16x2_f32x2(r[j], one_h2, nt);     // r - t, one rounding
         const f32x2 vj = fma_f16x2_f32x2(r[j], mone_h2, t[j]);  // t - r, one rounding
-        unpack2(uj, u[2 * j], u[2 * j + 1]);
-        unpack2(vj, v[2 * j], v[2 * j + 1]);
+        unpack2(uj, uu[2 * j], uu[2 * j + 1]);
+        unpack2(vj, vv[2 * j], vv[2 * j + 1]);
       }
-      const uint32_t su = sign_nibbles(u), sv = sign_nibbles(v);
+      const uint32_t su = sign_nibbles(uu), sv = sign_nibbles(vv);
       const uint32_t st = rtn & 0x88888888u;                        // sign of t (bit 3)
       const uint32_t away = (st & su) | (~st & sv);                 // bit 3 meaningful
       const uint32_t toward = (st & sv) | (~st & su);
       const uint32_t mag = rtn & 0x77777777u;
-      const uint32_t rg = ref | 0x88888888u;
+      const uint32_t rg = ref[k] | 0x88888888u;
       const uint32_t ge = rg - mag;                                 // bit 3: R >= m
       const uint32_t gt = rg - mag - 0x11111111u;                   // bit 3: R > m
-      const uint32_t other = rtn ^ ref;                             // bit 3: R on the other side
+      const uint32_t other = rtn ^ ref[k];                          // bit 3: R on the other side
       const uint32_t down = away & (~ge | other) & 0x88888888u;
       const uint32_t up = toward & gt & ~other & 0x88888888u;
-      out[g] = rtn + (up >> 3) - (down >> 3);
+      __stcs(out + g, rtn + (up >> 3) - (down >> 3));
     }
   }
 }
@@ -693,17 +727,26 @@ cudaError_t launch_quantize_guided(int mode, const GuidedParams& p, cudaStream_t
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
-  int64_t grid = (p.rows + 7) / 8;
-  const int64_t cap = static_cast<int64_t>(sm_count(device)) * 8;
+  // The guided encoder keeps the rollout's scales: only M (mode six or not) matters.
+  auto kern = mode == kModeSix ? guided_kernel<kModeSix> : guided_kernel<kModeFourOverSix>;
+  // One wave of resident blocks; the kernel spreads the work units over its warps.
+  static std::atomic<int> per_sm_cache[2] = {{0}, {0}};
+  std::atomic<int>& cached = per_sm_cache[mode == kModeSix ? 0 : 1];
+  int per_sm = cached.load();
+  if (per_sm == 0) {
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    cached.store(per_sm);
+  }
+  const int64_t units = p.rows * ((p.cols / 8 + 32 * kGuidedUnroll - 1) / (32 * kGuidedUnroll));
+  int64_t grid = (units + 7) / 8;  // 8 warps per block
+  const int64_t cap = static_cast<int64_t>(sm_count(device)) * per_sm;
   if (grid > cap) grid = cap;
   const LaunchOverride ov = launch_override();
   if (ov.max_ctas > 0 && grid > ov.max_ctas) grid = ov.max_ctas;
   if (grid < 1) grid = 1;
-  // The guided encoder keeps the rollout's scales: only M (mode six or not) matters.
-  if (mode == kModeSix)
-    guided_kernel<kModeSix><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
-  else
-    guided_kernel<kModeFourOverSix><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
+  kern<<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
