@@ -555,8 +555,19 @@ __global__ void __launch_bounds__(256) row_amax_kernel(const uint16_t* x, int64_
   const int64_t NW = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t row = gw; row < rows; row += NW) {
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * cols);
+    const int nvec = cols / 8;
     uint32_t m2 = 0;
-    for (int g = lane; g < cols / 8; g += 32) {
+    int g = lane;
+    for (; g + 96 < nvec; g += 128) {  // four independent 16-byte loads in flight per lane
+      uint4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = __ldcs(xr + g + 32 * k);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        m2 = max_abs_bf16x2(m2, max_abs_bf16x2(max_abs_bf16x2(v[k].x, v[k].y),
+                                               max_abs_bf16x2(v[k].z, v[k].w)));
+    }
+    for (; g < nvec; g += 32) {
       const uint4 v = __ldcs(xr + g);
       m2 = max_abs_bf16x2(m2, max_abs_bf16x2(max_abs_bf16x2(v.x, v.y), max_abs_bf16x2(v.z, v.w)));
     }
