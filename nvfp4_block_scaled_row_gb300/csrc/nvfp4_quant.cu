@@ -592,7 +592,7 @@ constexpr uint32_t kTargetSlotBytes = 8192;  // split rows wider than this acros
 
 // Team size, ring depth and warps per CTA for rows of `cols` elements: as many warps as shared
 // memory allows (up to 16), then as many stages as fit (up to 4, at least 2 when possible).
-bool choose_ring(int64_t cols, RingShape* out) {
+bool choose_ring(int64_t cols, RingShape* out, int warps_cap = 0) {
   if (cols <= 0 || cols % kBlockElems != 0 || cols > kMaxCols) return false;
   const int nblk = static_cast<int>(cols / kBlockElems);
   int team = 1;
@@ -604,6 +604,7 @@ bool choose_ring(int64_t cols, RingShape* out) {
   const LaunchOverride ov = launch_override();
   int max_warps = kMaxWarpsPerCta;
   if (ov.warps_per_cta > 0) max_warps = ov.warps_per_cta < team ? team : ov.warps_per_cta;
+  else if (warps_cap > 0 && warps_cap < max_warps) max_warps = warps_cap < team ? team : warps_cap;
   max_warps -= max_warps % team;
   for (int min_stages : {2, 1}) {
     for (int warps = max_warps; warps >= team; warps -= team) {
@@ -644,6 +645,17 @@ cudaError_t launch_impl(QuantParams p, cudaStream_t stream, bool after_amax_kern
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
+  {
+    // Too few rows to give every SM a full CTA: spread them over all SMs with smaller CTAs, so
+    // each SM runs few warps (fast per row) instead of some SMs running 16 and the rest idling.
+    const int64_t sms = sm_count(device);
+    const int64_t teams_full = rs.warps / rs.team;
+    if ((p.rows + teams_full - 1) / teams_full < sms) {
+      const int64_t teams_needed = (p.rows + sms - 1) / sms;
+      if (!choose_ring(p.cols, &rs, static_cast<int>(teams_needed * rs.team)))
+        return cudaErrorInvalidValue;
+    }
+  }
   const bool cached_dev = device >= 0 && device < LaunchCache::kDevices;
   if (!cached_dev || cache.attr_set[device].load() == 0) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
