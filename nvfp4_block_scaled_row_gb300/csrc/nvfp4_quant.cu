@@ -628,7 +628,7 @@ bool choose_ring(int64_t cols, RingShape* out, int warps_cap = 0) {
 // resident CTAs per SM for each launch shape seen (looked up once, then reused).
 struct LaunchCache {
   static constexpr int kDevices = 64;
-  static constexpr int kShapes = 8;
+  static constexpr int kShapes = 32;
   std::atomic<int> attr_set[kDevices];
   struct Entry {
     std::atomic<long long> key;  // warps | stages << 8 | slot_bytes << 16, 0 = empty

@@ -500,3 +500,43 @@ def test_gemm_nt_matches_float64_product(m, n, k):
     bad = np.abs(got - ref) > bound
     assert not bad.any(), f"{bad.sum()} of {bad.size} outputs off; worst {np.abs(got - ref)[bad].max()}"
     assert nv.nvfp4_get_device_status() == 0
+
+
+def test_device_calls_capture_into_cuda_graphs():
+    """Every device entry point can be captured into a CUDA graph (no host synchronisation or
+    allocation inside the library) and the replay reproduces the eager outputs."""
+    x = synth.generate(2, device=DEV, rows=700)["x"]
+    w = synth.generate(1, device=DEV, rows=256)["x"]
+    eager = {
+        "row": nv.nvfp4_quantize_rowwise(x),
+        "fused": nv.nvfp4_fused_roundtrip(x),
+        "fused_t": nv.nvfp4_fused_roundtrip(x, "tensor"),
+        "tensor": nv.nvfp4_quantize_tensor(w),
+        "residual": sum(nv.nvfp4_quantize_residual(x), ()),
+    }
+    amax = nv.nvfp4_row_amax(x)
+    eager["guided"] = (nv.nvfp4_quantize_guided(x, amax, eager["row"][0], eager["row"][1]),)
+    eager["deq"] = (nv.nvfp4_dequantize(*eager["row"]),)
+    torch.cuda.synchronize()
+    outs = {k: tuple(torch.empty_like(t) for t in v) for k, v in eager.items()}
+    ws = [torch.empty(nv.nvfp4_tensor_workspace_bytes(), dtype=torch.uint8, device=DEV)
+          for _ in range(2)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        nv.nvfp4_quantize_rowwise(x, "four_over_six", None, *outs["row"])
+        nv.nvfp4_fused_roundtrip(x, "row", "four_over_six", *outs["fused"])
+        nv.nvfp4_fused_roundtrip(x, "tensor", "four_over_six", *outs["fused_t"], ws[0])
+        nv.nvfp4_quantize_tensor(w, "four_over_six", *outs["tensor"], ws[1])
+        nv.nvfp4_dequantize(*eager["row"], "row", outs["deq"][0])
+        nv.nvfp4_quantize_guided(x, amax, eager["row"][0], eager["row"][1], "four_over_six",
+                                 outs["guided"][0])
+        outs["residual"] = sum(nv.nvfp4_quantize_residual(x), ())  # graph-pool outputs
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for k in ("row", "fused", "fused_t", "tensor", "deq", "guided", "residual"):
+        for a, b in zip(eager[k], outs[k]):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), k
+    assert nv.nvfp4_get_device_status() == 0
