@@ -187,13 +187,13 @@ __device__ __forceinline__ void encode_block(const uint4 A, const uint4 B, float
   }
 }
 
-// BF16 residual pair bf16(fp32(x) - fp32(y)) of two BF16 pairs (the difference is exact in FP32).
+// BF16 residual pair bf16(fp32(x) - fp32(y)) of two BF16 pairs.  x - y is exact in FP32 (y is
+// zero or within a few binades of x), so one BF16 FMA y * (-1) + x, which rounds the exact
+// result once, gives the same bits.
 __device__ __forceinline__ uint32_t bf16x2_residual(uint32_t xw, uint32_t yw) {
-  const uint16_t one_bf16 = 0x3F80;
-  const float neg_zero = -0.0f;
-  const f32x2 xf = bf16x2_to_f32x2_fma(xw, one_bf16, neg_zero);
-  const f32x2 yf = bf16x2_to_f32x2_fma(yw, one_bf16, neg_zero);
-  return bf16x2_from_f32x2(fma2(yf, pack2(-1.0f, -1.0f), xf));
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(yw), "r"(0xBF80BF80u), "r"(xw));
+  return d;
 }
 
 // Both halves of the result hold the largest |value| of a BF16 pair word (sign bits arbitrary).
