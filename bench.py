@@ -69,7 +69,8 @@ def fp4_tensor_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
-            return 6.0 * float(json.load(f)["bf16_tflops"]), "measured bf16_tflops x 6 (nominal fp4/bf16)"
+            bf16 = float(json.load(f)["bf16_tflops"])
+        return 6.0 * bf16, "measured bf16_tflops x 6 (nominal fp4/bf16)"
     except (OSError, KeyError, ValueError):
         return 6.0 * 1900.0, "fallback 1.9 PFLOP/s bf16 x 6 (nominal fp4/bf16)"
 
@@ -470,8 +471,10 @@ def main():
         "config": {"workload": f"{w.name} (workload {w.index}): {w.summary}",
                    "rows": rows, "cols": cols, "op": "fused quantize->dequantize round trip",
                    "scale": "row (per-token)", "mode": "four_over_six",
-                   "l2": f"inputs larger than L2 ({rows * cols * 2 / 1e6:.0f} MB > 129 MB), no flush",
-                   "timing": "K steps captured in one CUDA graph, one replay timed with CUDA events",
+                   "l2": f"inputs larger than L2 ({rows * cols * 2 / 1e6:.0f} MB > 129 MB), "
+                         "no flush",
+                   "timing": "K steps captured in one CUDA graph, one replay timed with CUDA "
+                             "events",
                    "parallelism": f"replicas x{world}"},
         "elem_per_s": round(world * rows * cols / (ms * 1e-3), 1),
         "frac_of_hbm_peak": round(achieved / peak, 4),
