@@ -18,6 +18,8 @@ constexpr int kDequantUnroll = 4;
 
 template <bool kTensor>
 __global__ void __launch_bounds__(kDequantWarps * 32) dequantize_kernel(const DequantParams p) {
+  pdl_wait();  // global memory only after the previous kernel on the stream
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kDequantWarps + (threadIdx.x >> 5);
   const int64_t NW = static_cast<int64_t>(gridDim.x) * kDequantWarps;
@@ -67,9 +69,11 @@ constexpr int kAmaxUnroll = 8;
 // Partial max |x| per CTA over a grid-strided range of 16-byte vectors, plus the scalar tail.
 __global__ void __launch_bounds__(kAmaxThreads) amax_partials_kernel(const uint16_t* x, int64_t n,
                                                                      float* partials) {
-  // The encoder that consumes the partials may start its own prologue (and its reads of x, which
-  // this kernel does not write) right away; it waits for this grid before reading the partials.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Global memory only after the previous kernel on the stream.  The encoder that consumes the
+  // partials may start its own prologue (and its reads of x, which this kernel does not write)
+  // right away; it waits for this grid before reading the partials.
+  pdl_wait();
+  pdl_trigger();
   const int64_t nvec = n / 8;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kAmaxThreads;
@@ -146,10 +150,10 @@ cudaError_t launch_dequantize(bool tensor_scale, const DequantParams& p, cudaStr
   if (ov.max_ctas > 0 && grid > ov.max_ctas) grid = ov.max_ctas;
   if (grid < 1) grid = 1;
   if (tensor_scale)
-    dequantize_kernel<true><<<static_cast<unsigned>(grid), kDequantWarps * 32, 0, stream>>>(p);
-  else
-    dequantize_kernel<false><<<static_cast<unsigned>(grid), kDequantWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+    return launch_programmatic(dequantize_kernel<true>, dim3(static_cast<unsigned>(grid)),
+                               dim3(kDequantWarps * 32), 0, stream, p);
+  return launch_programmatic(dequantize_kernel<false>, dim3(static_cast<unsigned>(grid)),
+                             dim3(kDequantWarps * 32), 0, stream, p);
 }
 
 cudaError_t launch_amax_partials(const uint16_t* x, int64_t n, float* partials, int* n_partials,
@@ -166,9 +170,9 @@ cudaError_t launch_amax_partials(const uint16_t* x, int64_t n, float* partials, 
   const LaunchOverride ov = launch_override();
   if (ov.max_ctas > 0 && grid > ov.max_ctas) grid = ov.max_ctas;
   if (grid < 1) grid = 1;
-  amax_partials_kernel<<<static_cast<unsigned>(grid), kAmaxThreads, 0, stream>>>(x, n, partials);
   *n_partials = static_cast<int>(grid);
-  return cudaGetLastError();
+  return launch_programmatic(amax_partials_kernel, dim3(static_cast<unsigned>(grid)),
+                             dim3(kAmaxThreads), 0, stream, x, n, partials);
 }
 
 cudaError_t launch_amax_partials_into(const uint16_t* x, int64_t n, float* partials, int capacity,
@@ -189,9 +193,9 @@ cudaError_t launch_amax_partials_into(const uint16_t* x, int64_t n, float* parti
     *too_small = true;
     return cudaSuccess;
   }
-  amax_partials_kernel<<<static_cast<unsigned>(grid), kAmaxThreads, 0, stream>>>(x, n, partials);
   *n_partials = static_cast<int>(grid);
-  return cudaGetLastError();
+  return launch_programmatic(amax_partials_kernel, dim3(static_cast<unsigned>(grid)),
+                             dim3(kAmaxThreads), 0, stream, x, n, partials);
 }
 
 cudaError_t launch_amax_finalize(const float* partials, int n, float* out, cudaStream_t stream) {

@@ -64,6 +64,7 @@ struct QuantParams {
   int32_t team;             // warps sharing one row
   int32_t blocks_per_warp;  // 16-element blocks each warp of a team owns
   uint32_t slot_bytes;      // bytes per ring slot (>= 32 * blocks_per_warp, multiple of 128)
+  int32_t prologue_before_wait;  // 1: the first row copies may precede griddepcontrol.wait
   int* status;              // device status word
   uint64_t timeout_ns;      // bound on every barrier wait
 };
@@ -387,6 +388,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // Named barrier over `threads` threads (a multiple of 32) of the CTA.
+// Programmatic dependent launch.  pdl_wait: global memory written or read by the previous kernel
+// on the stream is safe to use after it (it returns at once for an ordinary launch).
+// pdl_trigger: the next kernel on the stream may start its own set-up.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

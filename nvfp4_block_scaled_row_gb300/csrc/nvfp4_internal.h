@@ -9,6 +9,24 @@
 
 namespace nvfp4 {
 
+// Launches `kern` as a programmatic dependent of the previous kernel on `stream`: its blocks may
+// start while that kernel finishes, and wait for it (pdl_wait) before touching global memory.
+template <typename... Params, typename... Args>
+cudaError_t launch_programmatic(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Launch-shape overrides (0 = automatic), set through nvfp4_set_launch_config.
 struct LaunchOverride {
   int warps_per_cta;

@@ -243,6 +243,11 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
     for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
   fence_barrier_init();
   __syncthreads();
+  // Everything above touched only this CTA's shared memory, so it overlaps the previous kernel's
+  // tail; global memory waits for that kernel (except the first row copies of a tensor-scale grid
+  // that follows our amax kernel, see below).
+  if (!p.prologue_before_wait) pdl_wait();
+  pdl_trigger();
 
   // Group offsets only need validating: every row is quantized independently of its group.
   if (p.offsets != nullptr && blockIdx.x == 0 && warp == 0) {
@@ -280,10 +285,9 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
 
   RowFactors f{};
   if (kTensor) {
-    // Tensor scale: this grid may be a programmatic dependent of the amax kernel (x is not written
-    // there, so the copies above may already run); the partial maxima need that grid complete.
-    // Launched the ordinary way, the wait returns at once.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Tensor scale right after the amax kernel: x is not written there, so the copies above may
+    // already run; the partial maxima need that grid complete.
+    if (p.prologue_before_wait) pdl_wait();
     float a = 0.0f;
     for (int i = lane; i < p.n_amax; i += 32) a = fmaxf(a, p.amax_src[i]);
 #pragma unroll
@@ -463,6 +467,8 @@ __global__ void __launch_bounds__(256) guided_kernel(const GuidedParams p) {
   __shared__ ScaleEntry tab[256];
   for (int i = threadIdx.x; i < 256; i += blockDim.x) tab[i] = make_scale_entry(i);
   __syncthreads();
+  pdl_wait();  // global memory only after the previous kernel on the stream
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t NW = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -699,25 +705,13 @@ cudaError_t launch_impl(QuantParams p, cudaStream_t stream, bool after_amax_kern
   p.team = rs.team;
   p.blocks_per_warp = rs.blocks_per_warp;
   p.slot_bytes = rs.slot_bytes;
-  if (!kTensor || !after_amax_kernel) {
-    kern<<<static_cast<unsigned>(grid), rs.warps * 32, rs.smem, stream>>>(p);
-    return cudaGetLastError();
-  }
-  // Tensor scale right after our amax kernel: launched as its programmatic dependent.  Only then,
-  // because the row copies issued before griddepcontrol.wait are safe only while the grid this
-  // one depends on does not write x (the amax kernel only reads it, and it started after
-  // everything before it on the stream had finished).
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(rs.warps * 32);
-  cfg.dynamicSmemBytes = rs.smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  // Every launch is a programmatic dependent of the previous kernel on the stream, so its set-up
+  // overlaps that kernel's tail.  Only a tensor-scale launch right after our amax kernel issues
+  // its first row copies before the wait: that grid only reads x, and it started after
+  // everything before it on the stream had finished.
+  p.prologue_before_wait = (kTensor && after_amax_kernel) ? 1 : 0;
+  return launch_programmatic(kern, dim3(static_cast<unsigned>(grid)), dim3(rs.warps * 32),
+                             rs.smem, stream, p);
 }
 
 // Picks the fixed-trip-count instantiation when the row's blocks split evenly into 4, 7 or 8 per
@@ -794,8 +788,7 @@ cudaError_t launch_quantize_guided(int mode, const GuidedParams& p, cudaStream_t
   const LaunchOverride ov = launch_override();
   if (ov.max_ctas > 0 && grid > ov.max_ctas) grid = ov.max_ctas;
   if (grid < 1) grid = 1;
-  kern<<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_programmatic(kern, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_row_amax(const uint16_t* x, int64_t rows, int cols, float* amax,
