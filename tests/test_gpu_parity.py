@@ -540,3 +540,43 @@ def test_device_calls_capture_into_cuda_graphs():
         for a, b in zip(eager[k], outs[k]):
             assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), k
     assert nv.nvfp4_get_device_status() == 0
+
+
+def test_programmatic_launch_waits_for_the_producer():
+    """Each library kernel starts as a programmatic dependent of the previous kernel on the stream;
+    it must still see everything that kernel wrote.  A torch kernel rewrites x in place right
+    before every call (eagerly and inside a CUDA graph); each call's outputs must match a call on
+    an unshared copy of the new x."""
+    x = synth.generate(2, device=DEV, rows=3000)["x"]
+    want = [nv.nvfp4_fused_roundtrip(x.neg() if i % 2 == 0 else x.clone()) for i in range(2)]
+    want_q = [nv.nvfp4_quantize_rowwise(x.neg() if i % 2 == 0 else x.clone()) for i in range(2)]
+    torch.cuda.synchronize()
+    outs = [tuple(torch.empty_like(t) for t in w) for w in want]
+    outs_q = [tuple(torch.empty_like(t) for t in w) for w in want_q]
+    for step in range(6):
+        x.neg_()  # the producer: rewrites x just before the consumer launch
+        nv.nvfp4_fused_roundtrip(x, "row", "four_over_six", *outs[step % 2])
+        nv.nvfp4_quantize_rowwise(x, "four_over_six", None, *outs_q[step % 2])
+        nv.nvfp4_dequantize(*outs_q[step % 2], "row", outs[step % 2][3])  # reads the line above
+    torch.cuda.synchronize()
+    for w, o in zip(want, outs):
+        for a, b in zip(w, o):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    for w, o in zip(want_q, outs_q):
+        for a, b in zip(w, o):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    # the same inside a captured graph
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        x.neg_()
+        nv.nvfp4_fused_roundtrip(x, "row", "four_over_six", *outs[0])
+        x.neg_()
+        nv.nvfp4_fused_roundtrip(x, "row", "four_over_six", *outs[1])
+    g.replay()
+    torch.cuda.synchronize()
+    for w, o in zip(want, outs):
+        for a, b in zip(w, o):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    assert nv.nvfp4_get_device_status() == 0
