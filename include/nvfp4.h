@@ -38,6 +38,12 @@
  *     recorded wins.
  *   - Non-finite inputs are outside the contract: they do not fault, their outputs are unspecified.
  *   - Results do not depend on the launch configuration, the stream or the rest of the batch.
+ *   - Kernels are launched as programmatic dependents of the previous kernel on `stream` (they
+ *     set up shared memory while it finishes, and wait for it before touching global memory) and
+ *     let the next kernel start early.  A kernel the caller launches after a call with
+ *     programmatic stream serialization must wait for its prerequisite grid
+ *     (griddepcontrol.wait / cudaGridDependencySynchronize) before reading the call's outputs,
+ *     as for any programmatic dependent; ordinary launches need nothing.
  */
 #ifndef NVFP4_GB300_H
 #define NVFP4_GB300_H
