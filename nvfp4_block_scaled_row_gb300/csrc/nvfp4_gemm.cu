@@ -41,23 +41,39 @@ __global__ void swizzle_scales_kernel(const uint8_t* __restrict__ in, int64_t ro
   }
 }
 
-// y = bf16(fp32(fp32(D * S_x[row]) * S_w)), D row-major FP32 [m][n].
-__global__ void scale_epilogue_kernel(const float* __restrict__ d, const float* __restrict__ sx,
-                                      const float* __restrict__ sw, int64_t m, int64_t n,
-                                      uint16_t* __restrict__ y) {
+// y = bf16(fp32(fp32(D * S_x[row]) * S_w)), D row-major FP32 [m][n] (n a multiple of 16).
+// A block per row at a time; each thread keeps kEpiUnroll independent 16-byte loads in flight.
+constexpr int kEpiThreads = 128;
+constexpr int kEpiUnroll = 4;
+
+__device__ __forceinline__ uint2 scale_to_bf16x4(const float4 v, float s, float w) {
+  const float a = __fmul_rn(__fmul_rn(v.x, s), w), b = __fmul_rn(__fmul_rn(v.y, s), w);
+  const float c = __fmul_rn(__fmul_rn(v.z, s), w), e = __fmul_rn(__fmul_rn(v.w, s), w);
+  uint32_t lo, hi;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(e), "f"(c));
+  return make_uint2(lo, hi);
+}
+
+__global__ void __launch_bounds__(kEpiThreads) scale_epilogue_kernel(
+    const float* __restrict__ d, const float* __restrict__ sx, const float* __restrict__ sw,
+    int64_t m, int64_t n, uint16_t* __restrict__ y) {
+  nvfp4::pdl_wait();  // D is the previous kernel's output
   const float w = sw[0];
-  const int64_t total4 = m * n / 4;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total4;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t row = (i * 4) / n;
+  const int n4 = static_cast<int>(n / 4);
+  for (int64_t row = blockIdx.x; row < m; row += gridDim.x) {
     const float s = sx[row];
-    const float4 v = reinterpret_cast<const float4*>(d)[i];
-    const float a = __fmul_rn(__fmul_rn(v.x, s), w), b = __fmul_rn(__fmul_rn(v.y, s), w);
-    const float c = __fmul_rn(__fmul_rn(v.z, s), w), e = __fmul_rn(__fmul_rn(v.w, s), w);
-    uint32_t lo, hi;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(b), "f"(a));
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(e), "f"(c));
-    reinterpret_cast<uint2*>(y)[i] = make_uint2(lo, hi);
+    const float4* dr = reinterpret_cast<const float4*>(d + row * n);
+    uint2* yr = reinterpret_cast<uint2*>(y + row * n);
+    int c = threadIdx.x;
+    for (; c + (kEpiUnroll - 1) * kEpiThreads < n4; c += kEpiUnroll * kEpiThreads) {
+      float4 v[kEpiUnroll];
+#pragma unroll
+      for (int u = 0; u < kEpiUnroll; ++u) v[u] = __ldcs(dr + c + u * kEpiThreads);
+#pragma unroll
+      for (int u = 0; u < kEpiUnroll; ++u) yr[c + u * kEpiThreads] = scale_to_bf16x4(v[u], s, w);
+    }
+    for (; c < n4; c += kEpiThreads) yr[c] = scale_to_bf16x4(__ldcs(dr + c), s, w);
   }
 }
 
@@ -180,13 +196,15 @@ extern "C" nvfp4_status nvfp4_gemm_nt(const uint8_t* x_codes, const uint8_t* x_s
                      workspace, lt_ws, s) != CUBLAS_STATUS_SUCCESS)
     goto done;
   {
-    int64_t grid = (m * n / 4 + 255) / 256;
+    int64_t grid = m;
     const int64_t cap = static_cast<int64_t>(nvfp4::sm_count(device)) * 16;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    scale_epilogue_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
-        d, x_row_scale, w_tensor_scale, m, n, static_cast<uint16_t*>(y));
-    if (cudaGetLastError() == cudaSuccess) result = NVFP4_OK;
+    if (nvfp4::launch_programmatic(scale_epilogue_kernel, dim3(static_cast<unsigned>(grid)),
+                                   dim3(kEpiThreads), 0, s, static_cast<const float*>(d),
+                                   x_row_scale, w_tensor_scale, m, n,
+                                   static_cast<uint16_t*>(y)) == cudaSuccess)
+      result = NVFP4_OK;
   }
 done:
   if (pref) cublasLtMatmulPreferenceDestroy(pref);
