@@ -222,7 +222,8 @@ size_t nvfp4_swizzled_scales_bytes(int64_t rows, int64_t cols);
  * GEMMs read: tiles of 128 rows x 4 scale columns (512 bytes), tiles row-major over
  * [ceil(rows/128)][ceil(cols/64)], the scale of (row r, scale column c) at byte
  * (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4) of its tile; padding is zero.
- * swizzled: device buffer of nvfp4_swizzled_scales_bytes(rows, cols) bytes. */
+ * swizzled: 16-byte aligned device buffer of nvfp4_swizzled_scales_bytes(rows, cols) bytes
+ * (NVFP4_ERR_ALIGNMENT otherwise). */
 nvfp4_status nvfp4_swizzle_block_scales(const uint8_t* block_scales, int64_t rows, int64_t cols,
                                         uint8_t* swizzled, nvfp4_stream_t stream);
 

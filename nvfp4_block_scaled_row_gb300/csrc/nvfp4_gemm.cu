@@ -26,18 +26,34 @@ constexpr size_t kLtWorkspace = 32ull << 20;  // cuBLASLt scratch inside the cal
 
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
-// One thread per output byte of the swizzled layout; padding bytes get 0.
+// One thread per 16-byte line of the swizzled layout: line r32 of tile (tr, tc) holds, for each
+// row quadrant q, the four scales of row tr*128 + q*32 + r32 at scale columns tc*4 .. tc*4+3
+// (padding 0).  Rows whose four scales are 4-byte aligned in the source are read as one word.
 __global__ void swizzle_scales_kernel(const uint8_t* __restrict__ in, int64_t rows, int64_t scols,
-                                      uint8_t* __restrict__ out, int64_t total, int64_t tiles_c) {
-  for (int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; o < total;
-       o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t tile = o >> 9;  // 512-byte tiles
-    const int within = static_cast<int>(o & 511);
+                                      uint8_t* __restrict__ out, int64_t lines, int64_t tiles_c) {
+  for (int64_t l = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; l < lines;
+       l += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = l >> 5;
+    const int r32 = static_cast<int>(l & 31);
     const int64_t tr = tile / tiles_c, tc = tile - tr * tiles_c;
-    const int r32 = within >> 4, quad = (within >> 2) & 3, c4 = within & 3;
-    const int64_t r = tr * 128 + quad * 32 + r32;
-    const int64_t c = tc * 4 + c4;
-    out[o] = (r < rows && c < scols) ? in[r * scols + c] : 0;
+    const int64_t c0 = tc * 4;
+    uint32_t word[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t r = tr * 128 + q * 32 + r32;
+      uint32_t w = 0;
+      if (r < rows) {
+        const uint8_t* src = in + r * scols + c0;
+        if (c0 + 4 <= scols && (reinterpret_cast<uintptr_t>(src) & 3) == 0) {
+          w = *reinterpret_cast<const uint32_t*>(src);
+        } else {
+          for (int k = 0; k < 4; ++k)
+            if (c0 + k < scols) w |= static_cast<uint32_t>(src[k]) << (8 * k);
+        }
+      }
+      word[q] = w;
+    }
+    reinterpret_cast<uint4*>(out)[l] = make_uint4(word[0], word[1], word[2], word[3]);
   }
 }
 
@@ -113,14 +129,16 @@ extern "C" nvfp4_status nvfp4_swizzle_block_scales(const uint8_t* block_scales, 
   const int64_t total = round_up(rows, 128) * round_up(scols, 4);
   const uintptr_t a = reinterpret_cast<uintptr_t>(block_scales), b = reinterpret_cast<uintptr_t>(swizzled);
   if (a < b + total && b < a + static_cast<uintptr_t>(rows * scols)) return NVFP4_ERR_INVALID_ARG;
+  if ((b & 15) != 0) return NVFP4_ERR_ALIGNMENT;  // written in 16-byte lines
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return NVFP4_ERR_CUDA;
-  int64_t grid = (total + 255) / 256;
+  const int64_t lines = total / 16;
+  int64_t grid = (lines + 255) / 256;
   const int64_t cap = static_cast<int64_t>(nvfp4::sm_count(device)) * 8;
   if (grid > cap) grid = cap;
   swizzle_scales_kernel<<<static_cast<unsigned>(grid), 256, 0,
                           reinterpret_cast<cudaStream_t>(stream)>>>(block_scales, rows, scols,
-                                                                    swizzled, total,
+                                                                    swizzled, lines,
                                                                     round_up(scols, 4) / 4);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }

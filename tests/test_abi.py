@@ -117,6 +117,22 @@ def test_dequantize_host_validation(lib):
     assert call(y=P((1 << 20) + 16)) == INVALID  # y overlaps the codes
 
 
+def test_swizzle_and_gemm_host_validation(lib):
+    sw = lib.nvfp4_swizzle_block_scales
+    assert sw(P(1 << 20), -1, 64, P(2 << 20), None) == INVALID
+    assert sw(P(1 << 20), 4, 40, P(2 << 20), None) == SHAPE
+    assert sw(None, 0, 64, None, None) == OK
+    assert sw(P(1 << 20), 4, 64, P((2 << 20) + 8), None) == ALIGN  # 16-byte lines
+    assert sw(P(1 << 20), 4, 64, P(1 << 20), None) == INVALID  # overlaps the input
+    g = lib.nvfp4_gemm_nt
+    ws = lib.nvfp4_gemm_workspace_bytes(256, 256)
+    ok = [P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20), P(6 << 20)]
+    assert g(*ok, 256, 256, 96, P(7 << 20), P(8 << 20), ws, None) == SHAPE  # k % 64
+    assert g(*ok, 256, 250, 128, P(7 << 20), P(8 << 20), ws, None) == SHAPE  # n % 16
+    assert g(*ok, 256, 256, 128, P((7 << 20) + 8), P(8 << 20), ws, None) == ALIGN
+    assert g(*ok, 256, 256, 128, P(7 << 20), P(8 << 20), ws - 1, None) == WORKSPACE
+
+
 def test_launch_config_validation(lib):
     assert lib.nvfp4_set_launch_config(-1, 0, 0) == INVALID
     assert lib.nvfp4_set_launch_config(0, 99, 0) == INVALID
