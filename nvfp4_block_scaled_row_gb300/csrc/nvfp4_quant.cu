@@ -196,6 +196,16 @@ __device__ __forceinline__ uint32_t bf16x2_residual(uint32_t xw, uint32_t yw) {
   return d;
 }
 
+// E2M1 codes of eight BF16 zeros (+0 or -0): the sign of each element in bit 3 of its nibble.
+__device__ __forceinline__ uint32_t sign_codes(const uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    out |= (((w[k] >> 12) & 0x8u) | ((w[k] >> 24) & 0x80u)) << (8 * k);
+  return out;
+}
+
 // Both halves of the result hold the largest |value| of a BF16 pair word (sign bits arbitrary).
 __device__ __forceinline__ float abs_max_word(uint32_t mx) {
   const uint32_t mm = max_abs_bf16x2(mx, __byte_perm(mx, 0, 0x1032));
@@ -375,6 +385,27 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
     uint8_t* scales_row = p.scales + row * nblk;
     uint32_t rmax[kMaxBlocksPerLane];
     uint32_t rm2 = 0;
+    if (!kResidual && f.S_dec == 0.0f) {
+      // Zero amax (a padding row, or an all-zero tensor): every element is +-0, so every scale
+      // is 0, every code is the sign of its element (0x0 or 0x8) and y = x, bit for bit.
+#pragma unroll
+      for (int j = 0; j < (kNB > 0 ? kNB : kMaxBlocksPerLane); ++j) {
+        const int b = b0 + lane + 32 * j;
+        if (kNB == 0 && b >= b1) break;
+        const unsigned char* blk = xs + (b - b0) * 32;
+        const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
+        const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
+        uint32_t* cw = reinterpret_cast<uint32_t*>(codes_row + b * 8);
+        cw[h0] = sign_codes(A);
+        cw[1 - h0] = sign_codes(B);
+        scales_row[b] = 0;
+        if (kFused) {
+          uint16_t* y_blk = p.y + row * cols + b * kBlockElems;
+          *reinterpret_cast<uint4*>(y_blk + h0 * 8) = A;
+          *reinterpret_cast<uint4*>(y_blk + (1 - h0) * 8) = B;
+        }
+      }
+    } else {
 #pragma unroll
     for (int j = 0; j < (kNB > 0 ? kNB : kMaxBlocksPerLane); ++j) {
       const int b = b0 + lane + 32 * j;
@@ -401,6 +432,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
         rmax[j] = block_max_word(RA, RB);
         rm2 = max_abs_bf16x2(rm2, rmax[j]);
       }
+    }
     }
 
     if (kResidual) {

@@ -580,3 +580,22 @@ def test_programmatic_launch_waits_for_the_producer():
         for a, b in zip(w, o):
             assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
     assert nv.nvfp4_get_device_status() == 0
+
+
+@pytest.mark.parametrize("cols", [7168, 2048, 528])
+def test_signed_zero_rows(cols):
+    """Rows whose amax is zero hold only +0 and -0: codes carry each element's sign, scales and
+    S_dec are zero and y reproduces x bit for bit (row and tensor scale, fused and separate)."""
+    rng = np.random.default_rng(cols)
+    rows = 40
+    bits = np.where(rng.random((rows, cols)) < 0.5, 0x8000, 0x0000).astype(np.uint16)
+    bits[3] = 0x8000  # an all -0 row
+    bits[4] = 0       # an all +0 row
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    x[5:9] = synth.generate(2, device=DEV, rows=4)["x"][:, :cols]  # some ordinary rows among them
+    check_rowwise(x)
+    check_rowwise(x, SIX)
+    c, s, d, y = nv.nvfp4_fused_roundtrip(x)
+    assert torch.equal(y[:5].view(torch.int16), x[:5].view(torch.int16))
+    zero_only = x[:5].contiguous()
+    check_tensor(zero_only)
