@@ -257,9 +257,10 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
   // tail; global memory waits for that kernel (except the first row copies of a tensor-scale grid
   // that follows our amax kernel, see below).
   if (!p.prologue_before_wait) {
-    // Fused round trip: while the previous kernel finishes, pull this warp's first rows into L2
-    // (coherent, so safe even if that kernel writes them); the copies after the wait then hit L2.
-    // (Measured: +2.3% on the round trip; quantize-only kernels lost 2% with it, so they skip it.)
+    // While the previous kernel finishes, pull this warp's first rows into L2 (coherent, so safe
+    // even if that kernel writes them); the copies after the wait then hit L2.  Measured: the
+    // fused round trip gains 2.3% prefetching all its ring's rows; quantize-only kernels lose 2%
+    // doing the same but gain 0.5-2.5% prefetching only the first row.  Residual kernels skip it.
     const int pb0 = (warp % TW) * p.blocks_per_warp;
     const int pb1 = min(p.cols / kBlockElems, pb0 + p.blocks_per_warp);
     const int64_t pgt = static_cast<int64_t>(blockIdx.x) * (nwarps / TW) + warp / TW;
@@ -268,6 +269,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
       for (int s = 0; s < S && pgt + s * pNT < p.rows; ++s)
         bulk_prefetch_l2(p.x + (pgt + s * pNT) * p.cols + pb0 * 16,
                          static_cast<uint32_t>(pb1 - pb0) * 32u);
+    if (!kFused && !kResidual && lane == 0 && pb1 > pb0 && pgt < p.rows)
+      bulk_prefetch_l2(p.x + pgt * p.cols + pb0 * 16, static_cast<uint32_t>(pb1 - pb0) * 32u);
     pdl_wait();
   }
   pdl_trigger();
