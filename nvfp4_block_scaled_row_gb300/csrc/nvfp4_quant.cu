@@ -515,8 +515,6 @@ __global__ void __launch_bounds__(256) guided_kernel(const GuidedParams p) {
   __shared__ ScaleEntry tab[256];
   for (int i = threadIdx.x; i < 256; i += blockDim.x) tab[i] = make_scale_entry(i);
   __syncthreads();
-  pdl_wait();  // global memory only after the previous kernel on the stream
-  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t NW = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -532,6 +530,14 @@ __global__ void __launch_bounds__(256) guided_kernel(const GuidedParams p) {
   const int64_t per_warp = (total + NW - 1) / NW;
   const int64_t u_begin = gw * per_warp;
   const int64_t u_end = min(total, u_begin + per_warp);
+  if (lane == 0 && u_begin < u_end) {  // this warp's first x bytes into L2 while the wait runs
+    const int64_t r0 = u_begin / units_per_row;
+    const int g0 = static_cast<int>(u_begin - r0 * units_per_row) * 32 * kGuidedUnroll;
+    const int n = min(ngroups - g0, 32 * kGuidedUnroll);
+    bulk_prefetch_l2(p.x + r0 * cols + g0 * 8, static_cast<uint32_t>(n) * 16u);
+  }
+  pdl_wait();  // global memory only after the previous kernel on the stream
+  pdl_trigger();
   int64_t cur_row = -1;
   f32x2 senc2 = pack2(0.0f, 0.0f);
   int64_t row = u_begin / units_per_row;  // walked forward below, without further divisions
