@@ -226,7 +226,8 @@ __device__ __forceinline__ uint32_t block_max_word(const uint4 A, const uint4 B)
 // warp per team the row amax is combined through shared memory behind a named barrier; if any
 // member's copy times out, all members leave together after that barrier.
 // kNB > 0: every lane owns exactly kNB blocks of each row (the row's blocks split evenly over the
-// team, 32 * kNB per warp), so the block loops have a fixed trip count; kNB = 0: any split.
+// team, 32 * kNB per warp), so the block loops have a fixed trip count (residual kernels: only
+// the third pass's loop); kNB = 0: any split.
 template <int kMode, bool kTensor, bool kFused, bool kResidual, int kNB>
 __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const QuantParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
       for (int j = 0; j < kMaxBlocksPerLane; ++j) {
         const int b = b0 + lane + 32 * j;
         bmax[j] = 0;
-        if (kNB > 0 ? j < kNB : (ok && b < b1)) {
+        if ((kNB > 0 && !kResidual) ? j < kNB : (ok && b < b1)) {
           const unsigned char* blk = xs + (b - b0) * 32;
           const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
           const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
@@ -410,9 +411,9 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
       }
     } else {
 #pragma unroll
-    for (int j = 0; j < (kNB > 0 ? kNB : kMaxBlocksPerLane); ++j) {
+    for (int j = 0; j < ((kNB > 0 && !kResidual) ? kNB : kMaxBlocksPerLane); ++j) {
       const int b = b0 + lane + 32 * j;
-      if (kNB == 0 && b >= b1) break;
+      if ((kNB == 0 || kResidual) && b >= b1) break;
       unsigned char* blk = xs + (b - b0) * 32;
       const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
       const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
@@ -770,11 +771,12 @@ cudaError_t launch_impl(QuantParams p, cudaStream_t stream, bool after_amax_kern
 
 // Picks the fixed-trip-count instantiation when the row's blocks split evenly into 4, 7 or 8 per
 // lane (widths 2048, 7168, 4096, 8192, 16384, ...).  Quantize-only kernels are issue-bound and
-// gain 2-6% from it (measured); the fused round trip (bound by HBM) is unchanged by it and the
-// residual kernel measured 3.6% slower with it, so both keep the general form.
+// gain 2-6% from it (measured); the fused round trip (bound by HBM) is unchanged by it and keeps
+// the general form; the residual kernel uses it for its third pass only (+1.5%; with it in the
+// first two passes as well it measured 3.6% slower).
 template <int kMode, bool kTensor, bool kFused, bool kResidual>
 cudaError_t launch_nb(QuantParams p, cudaStream_t stream, bool after_amax_kernel = false) {
-  if constexpr (!kFused && !kResidual) {
+  if constexpr (!kFused) {  // quantize-only and residual kernels
     RingShape rs;
     if (!choose_ring(p.cols, &rs)) return cudaErrorInvalidValue;
     const int nblk = p.cols / kBlockElems;
