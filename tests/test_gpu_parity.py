@@ -599,3 +599,40 @@ def test_signed_zero_rows(cols):
     assert torch.equal(y[:5].view(torch.int16), x[:5].view(torch.int16))
     zero_only = x[:5].contiguous()
     check_tensor(zero_only)
+
+
+def test_concurrent_host_threads_device_calls():
+    """Host threads calling the device entry points at once, each on its own stream, with launch
+    shapes seen for the first time (the per-device launch caches fill concurrently): every
+    output equals the single-threaded result."""
+    import threading
+
+    inputs = [synth.generate(2, device=DEV, rows=r)["x"] for r in (97, 513, 1500, 2222)]
+    wants = [nv.nvfp4_fused_roundtrip(x) for x in inputs]
+    wants_t = [nv.nvfp4_quantize_tensor(x) for x in inputs]
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(i):
+        try:
+            torch.cuda.set_device(0)
+            st = torch.cuda.Stream()
+            x = inputs[i]
+            with torch.cuda.stream(st):
+                for _ in range(20):
+                    got = nv.nvfp4_fused_roundtrip(x)
+                    got_t = nv.nvfp4_quantize_tensor(x)
+            st.synchronize()
+            for a, b in zip(wants[i] + wants_t[i], got + got_t):
+                if not torch.equal(a.view(torch.uint8), b.view(torch.uint8)):
+                    errors.append(i)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(len(inputs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert nv.nvfp4_get_device_status() == 0
