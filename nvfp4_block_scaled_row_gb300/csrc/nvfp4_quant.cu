@@ -2,14 +2,18 @@
 // or per-tensor FP32 scale, E4M3 block scales with Four-Over-Six selection (Sec. 4), packed E2M1
 // codes, and optionally the BF16 dequantized round trip (Sec. 3) in the same pass.
 //
-// Shape of the computation.  The path is bound by HBM bandwidth: every element is read once (2 B)
-// and written once (0.5625 B, plus 2 B for the round trip).  A persistent grid of warps walks the
-// rows; each warp owns a ring of shared-memory slots, one BF16 row per slot, filled by bulk
-// asynchronous copies (cp.async.bulk, the non-tensor TMA path) that complete on per-slot
-// mbarriers.  While the warp encodes row k, rows k+1 .. k+stages-1 are in flight.  Per row:
-//   pass 1  row amax from shared memory (packed BF16x2 |max|, then a warp shuffle reduction);
+// Shape of the computation.  Every element is read once (2 B) and written once (0.5625 B, plus
+// 2 B for the round trip).  A persistent grid (one CTA of 16 warps per SM) walks the rows in
+// teams of warps that share a row, each warp owning a contiguous part of it.  Each warp owns a
+// ring of shared-memory slots, one part-row per slot, filled by bulk asynchronous copies
+// (cp.async.bulk, the non-tensor TMA path) that complete on per-slot mbarriers: while the warp
+// encodes row k, its parts of the next rows are in flight.  Per row:
+//   pass 1  row amax from shared memory (packed BF16x2 |max|, warp shuffle, then the team's
+//           partial maxima through shared memory);
 //   pass 2  one lane per 16-element block: block amax, both candidate E4M3 scales, E2M1 codes
 //           for both candidates, their block squared errors, the 4/6 choice, and the stores.
+// Each launch is a programmatic dependent of the previous kernel on the stream: shared-memory
+// set-up (and an L2 prefetch of the first rows) overlaps that kernel's tail.
 // Lanes of a quarter-warp read alternate 16-byte halves of their 32-byte blocks first, which
 // keeps every 128-bit shared-memory read free of bank conflicts.  The errors are summed in the
 // fixed order the spec prescribes (four FMA chains, then a pairwise combine), so the result is
