@@ -10,6 +10,8 @@ from oracle import build as obuild
 from nvfp4_block_scaled_row_gb300 import synth
 
 import test_oracle_formats as F
+import test_oracle_fp16_selector as H
+import test_oracle_guided as T
 import test_oracle_method as M
 import test_oracle_residual as R
 
@@ -38,6 +40,13 @@ MUTATIONS = [
     ("residual not rounded to bf16",
      "dx[k] = oracle_bf16_encode(oracle_bf16_to_f32(xr[k]) - oracle_bf16_to_f32(y[k]));",
      "dx[k] = (uint16_t)(oracle_bf16_encode(oracle_bf16_to_f32(xr[k])) - y[k]);"),
+    ("S_enc = M/a", "out[0] = clamp_to_finite((6.0f * M) / a); /* S_enc */",
+     "out[0] = clamp_to_finite(M / a); /* S_enc */"),
+    ("guided ignores the rollout", "double v = (fabs(hi - rv) < fabs(lo - rv)) ? hi : lo;",
+     "double v = (fabs(hi - tc) < fabs(lo - tc)) ? hi : lo;"),
+    ("guided takes the farther neighbour", "double v = (fabs(hi - rv) < fabs(lo - rv)) ? hi : lo;",
+     "double v = (fabs(hi - rv) < fabs(lo - rv)) ? lo : hi;"),
+    ("fp16 error scaled by s", "return (float)Eh * (s * s);", "return (float)Eh * s;"),
 ]
 
 
@@ -69,6 +78,11 @@ def _pins(inputs):
     M.test_dequant_closed_form(inputs)
     R.test_residual_is_quantize_of_independent_residual(inputs, oracle.MODE_FOUR_OVER_SIX)
     R.test_residual_recovers_most_of_the_error(inputs)
+    T.test_trace_worked_example()
+    T.test_identity_when_trainer_matches_rollout()
+    T.test_choice_is_a_neighbour_and_never_further_than_rtn(1)
+    H.test_outputs_differ_only_where_the_choice_flips(inputs)
+    H.test_choice_agreement_with_fp32(inputs)
 
 
 @pytest.fixture(scope="module")
