@@ -47,7 +47,7 @@ def test_sharded_tensor_and_row_paths_match_unsharded():
     xb = synth.as_u16(d["x"])
     offsets = d["offsets"]
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.start_processes(_worker, args=(port, xb, offsets, results), nprocs=WORLD,
                            start_method="spawn", join=True)
