@@ -34,9 +34,8 @@
  *   - s_T = E4M3(RNE, saturating)(fp32(m * c_T)), m the block amax, T in {6, 4};
  *   - target z = fp32(x * S_enc); scaled-down target t = fp32(z * fp32(1/s_T)) (0 when s_T == 0);
  *   - E2M1 rounding is RTN with ties to the even mantissa bit, saturating at 6, sign of t kept;
- *   - block error e_T = sum of (z - r*s_T)^2 in FP32: d = fma(-r, s_T, z); four fma chains over the
- *     elements {8h+p, 8h+p+2, 8h+p+4, 8h+p+6} (h = half, p = parity), combined as
- *     (E[0][0] + E[0][1]) + (E[1][0] + E[1][1]);
+ *   - block error e_T = sum of (z - r*s_T)^2 in FP32: d_i = fma(-r_i, s_T, z_i), then
+ *     e = 0; e = fma(d_i, d_i, e) for i = 0, 1, ..., 15 (one chain, ascending element order);
  *   - T = 4 iff mode is four_over_six and e_4 < e_6 (ties go to 6);
  *   - dequant y = bf16_RNE(fp32(fp32(r * s) * S_dec));
  *   - codes: row-major [rows][cols/2], element 2j in the low nibble of byte j;
@@ -198,17 +197,10 @@ static int quantize_candidate(const float x[ORACLE_BLOCK], float m, float S_enc,
     code_out[i] = (uint8_t)code;
     d[i] = fmaf(-r, s, z);    /* r*s is exact in FP32 */
   }
-  float E[2][2];
-  for (int h = 0; h < 2; ++h)
-    for (int p = 0; p < 2; ++p) {
-      float acc = 0.0f;
-      for (int k = 0; k < 4; ++k) {
-        float di = d[8 * h + p + 2 * k];
-        acc = fmaf(di, di, acc);
-      }
-      E[h][p] = acc;
-    }
-  *err_out = (E[0][0] + E[0][1]) + (E[1][0] + E[1][1]);
+  /* The block squared error, summed from +0 over the elements in ascending order, one fma each. */
+  float e = 0.0f;
+  for (int i = 0; i < ORACLE_BLOCK; ++i) e = fmaf(d[i], d[i], e);
+  *err_out = e;
   return sbyte;
 }
 

@@ -145,6 +145,48 @@ def test_ties_go_to_six():
     assert out["scales"][0, 0] == 0
 
 
+def chain_order_row():
+    """One row of two blocks whose 4/6 choice is decided by the order of the error sum.
+
+    The row amax is 1536, so in mode four_over_six S_enc = 6 * 256 / 1536 = 1 and the targets are
+    the inputs themselves.  Both blocks hold the max (block scales: scale-to-6 256, scale-to-4 384,
+    so the candidate grids are {0, 128, 256, 384, 512, 768, 1024, 1536} and {0, 192, 384, 576,
+    768, 1152, 1536}), thirteen values eps = 2^-7 (zero codes under both candidates, residual eps),
+    and the pair 576, 512: 576 is on the scale-to-4 grid and 64 from the scale-to-6 grid, 512 the
+    other way round.  Block 0 is [576, 1536, eps x 13, 512], block 1 the mirror [512, 1536, eps x
+    13, 576].  So each block has one residual of 64 and thirteen of eps under each candidate: the
+    exact sums are equal (4096 + 13 * 2^-14), and only the FP32 rounding of the chain separates
+    them.  The FP32 ulp at 4096 is 2^-11 = 8 * 2^-14:
+      - a chain that meets the 64 first stays at 4096 (each eps^2 = 2^-14 is an eighth of an ulp);
+      - a chain that meets it last adds 4096 to 13 * 2^-14 = 1.625 ulp once, giving 4096 + 2^-10.
+    Summed in ascending element order, block 0's scale-to-6 chain meets its 64 first and its
+    scale-to-4 chain meets it last, so e6 = 4096 < e4 = 4096 + 2^-10 and 6 is chosen; block 1 is
+    the other way round and chooses 4.  Descending order reverses both choices; four interleaved
+    chains over every second element of each half (combined pairwise) tie block 1 and send it to 6.
+    """
+    eps = 2.0 ** -7
+    b0 = [576.0, 1536.0] + [eps] * 13 + [512.0]
+    b1 = [512.0, 1536.0] + [eps] * 13 + [576.0]
+    return _bits(np.array(b0 + b1, np.float32))[None, :]
+
+
+def test_block_error_is_one_ascending_chain():
+    """The block error is e = fma(d_i, d_i, e) over i = 0..15 from +0: the closed-form values of
+    chain_order_row (derived in its docstring) pin the order, the choices and the error bits."""
+    xb = chain_order_row()
+    out = oracle.quantize(xb, F4, diagnostics=True)
+    assert out["scale"][0] == np.float32(1536.0 / 1536.0)
+    assert list(out["choice"][0]) == [0, 1]
+    lo, hi = np.float32(4096.0), np.float32(4096.0 + 2.0 ** -10)
+    assert out["errs"][0, 0].tolist() == [lo, hi]
+    assert out["errs"][0, 1].tolist() == [hi, lo]
+    # Scale bytes: E4M3 256 = 0x78 (scale-to-6) for block 0, E4M3 384 = 0x7C (scale-to-4) for 1.
+    assert list(out["scales"][0]) == [0x78, 0x7C]
+    nib = unpack_codes(out["codes"])[0]
+    assert list(nib[:16]) == [4, 7] + [0] * 13 + [4]    # 576 -> 2 * 256, 1536 -> 6, 512 -> 2
+    assert list(nib[16:]) == [3, 6] + [0] * 13 + [3]    # 512, 576 -> 1.5 * 384, 1536 -> 4 * 384
+
+
 def test_per_element_codes_are_nearest(inputs):
     """Given the chosen scale, every code is the nearest codeword to the scaled target."""
     xb = inputs[0][:64]

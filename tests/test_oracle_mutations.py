@@ -27,7 +27,17 @@ MUTATIONS = [
     ("S_dec = 1/S_enc", "out[3] = a / (6.0f * M);", "out[3] = 1.0f / out[0];"),
     ("ties go to 4", "pick4 = e4 < e6; /* ties go to 6 */", "pick4 = e4 <= e6; /* ties go to 6 */"),
     ("residual sign", "d[i] = fmaf(-r, s, z);", "d[i] = fmaf(r, s, z);"),
-    ("error chain index", "float di = d[8 * h + p + 2 * k];", "float di = d[8 * h + p + k];"),
+    ("error chain index", "for (int i = 0; i < ORACLE_BLOCK; ++i) e = fmaf(d[i], d[i], e);",
+     "for (int i = 0; i < ORACLE_BLOCK; ++i) e = fmaf(d[i], d[i ^ 1], e);"),
+    ("error chain descending", "for (int i = 0; i < ORACLE_BLOCK; ++i) e = fmaf(d[i], d[i], e);",
+     "for (int i = ORACLE_BLOCK - 1; i >= 0; --i) e = fmaf(d[i], d[i], e);"),
+    ("error chain in two halves", "for (int i = 0; i < ORACLE_BLOCK; ++i) e = fmaf(d[i], d[i], e);",
+     "float h1 = 0.0f; for (int i = 0; i < 8; ++i) { e = fmaf(d[i], d[i], e); "
+     "h1 = fmaf(d[8 + i], d[8 + i], h1); } e = e + h1;"),
+    ("error chain four interleaved", "for (int i = 0; i < ORACLE_BLOCK; ++i) e = fmaf(d[i], d[i], e);",
+     "float E[4] = {0.0f, 0.0f, 0.0f, 0.0f}; for (int i = 0; i < ORACLE_BLOCK; ++i) "
+     "E[(i >> 3) * 2 + (i & 1)] = fmaf(d[i], d[i], E[(i >> 3) * 2 + (i & 1)]); "
+     "e = (E[0] + E[1]) + (E[2] + E[3]);"),
     ("nibble order", "packed[j] = (uint8_t)(c[2 * j] | (c[2 * j + 1] << 4));",
      "packed[j] = (uint8_t)(c[2 * j + 1] | (c[2 * j] << 4));"),
     ("block amax over 8", "for (int i = 0; i < ORACLE_BLOCK; ++i) m = fmaxf(m, fabsf(x[i]));",
@@ -71,6 +81,7 @@ def _pins(inputs):
     M.test_page_example_five_sixths_prefers_four()
     M.test_four_over_six_choice_agrees_with_float64(inputs)
     M.test_ties_go_to_six()
+    M.test_block_error_is_one_ascending_chain()
     M.test_per_element_codes_are_nearest(inputs)
     for four in (False, True):
         M.test_idempotent_on_grid_values(four)
