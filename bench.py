@@ -1,11 +1,12 @@
 #!/usr/bin/env python
 """Throughput of the GB300 NVFP4 4/6 quantizer, as one JSON line.
 
-Headline workload: MoE activations at DeepSeek-V3 width, X bf16 [16384 x 7168], per-token FP32
-scale, Four-Over-Six block scales, fused quantize -> dequantize round trip (codes, E4M3 scales,
-row scales and BF16 y), i.e. one launch of nvfp4_fused_roundtrip per step.  Inputs are drawn on
-the device (seeded) and stay resident; the 235 MB input exceeds the 129 MB L2, so no step reads
-the previous step's data from L2.
+Headline workload: the long-rollout batch, X bf16 [131072 x 7168] (Student-t(4) entries, 10%
+all-zero rows, 1% rows with one +-3e4 spike), per-token FP32 scale, Four-Over-Six block scales,
+fused quantize -> dequantize round trip (codes, E4M3 scales, row scales and BF16 y), i.e. one
+launch of nvfp4_fused_roundtrip per step: the largest of the five workloads.  Inputs are drawn
+on the device (seeded) and stay resident; the 1.88 GB input exceeds the 129 MB L2, so no step
+reads the previous step's data from L2.
 
   value     algorithmic HBM bytes (2 B in + 0.5625 B codes/scales + 2 B y per element + 4 B per
             row) per step / device time per step, summed over ranks, in GB/s; the K timed steps
@@ -13,8 +14,9 @@ the previous step's data from L2.
   e2e       the same metric through the public API with pinned host buffers: every step copies
             x host->device, runs the call, and copies all outputs back
   roofline  the fused kernel's achieved GB/s against the measured HBM copy bandwidth
-  cpu_baseline  the CPU oracle on a bounded sample of the same rows (single thread)
-  also      kernel-only GB/s of the other workloads (weights, expert-grouped, long rollout)
+  cpu_baseline  the CPU oracle on a bounded sample of the same rows (all host cores, and one)
+  also      kernel-only GB/s of the other workloads and operations
+  cpu_baselines the CPU oracle on a bounded sample of every workload (all host cores, and one)
 
 --impl reference times the CPU oracle instead (the only reference this method has).
 Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no collective on the path).
@@ -32,7 +34,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-HEADLINE = 2
+HEADLINE = 4
 METRIC = "NVFP4 4/6 quantize GB/s and elem/s, fraction of GB300 HBM peak"
 L2_BYTES = 129 * 1024 * 1024
 
@@ -226,15 +228,19 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def oracle_pass(x_u16, op, threads):
+def oracle_pass(x_u16, op, threads, scale_kind="row", mode="four_over_six"):
     """The oracle on the rows of x_u16, split into `threads` contiguous row ranges run at once
     (the ctypes calls release the GIL, so each range runs on its own core)."""
     import oracle
 
+    omode = {"six": oracle.MODE_SIX, "four_over_six": oracle.MODE_FOUR_OVER_SIX,
+             "four_over_six_fp16": oracle.MODE_FOUR_OVER_SIX_FP16}[mode]
+    okind = oracle.SCALE_TENSOR if scale_kind == "tensor" else oracle.SCALE_ROW
+
     def one(part):
-        out = oracle.quantize(part, oracle.MODE_FOUR_OVER_SIX)
+        out = oracle.quantize(part, omode, okind)
         if op != "quantize":
-            oracle.dequantize(out["codes"], out["scales"], out["scale"])
+            oracle.dequantize(out["codes"], out["scales"], out["scale"], okind)
 
     if threads <= 1:
         one(x_u16)
@@ -247,9 +253,9 @@ def oracle_pass(x_u16, op, threads):
         list(pool.map(one, parts))
 
 
-def cpu_baseline(x, op, seconds):
+def cpu_baseline(x, op, seconds, scale_kind="row", mode="four_over_six"):
     """The oracle, as it stands, on bounded samples of rows of x: once on one thread, once on all
-    host cores (the reported value)."""
+    host cores (the reported value).  Each sample is sized for about seconds / 2 of CPU time."""
     import numpy as np
 
     from nvfp4_block_scaled_row_gb300 import synth
@@ -257,7 +263,7 @@ def cpu_baseline(x, op, seconds):
     rows, cols = x.shape
     probe = synth.as_u16(x[:2])
     t0 = time.perf_counter()
-    oracle_pass(probe, op, 1)
+    oracle_pass(probe, op, 1, scale_kind, mode)
     per_row = (time.perf_counter() - t0) / 2
     cores = host_cores()
     res = {}
@@ -266,9 +272,9 @@ def cpu_baseline(x, op, seconds):
         idx = np.linspace(0, rows - 1, n).astype(np.int64)
         sample = synth.as_u16(x[torch.as_tensor(idx, device=x.device)])
         t0 = time.perf_counter()
-        oracle_pass(sample, op, threads)
+        oracle_pass(sample, op, threads, scale_kind, mode)
         dt = time.perf_counter() - t0
-        res[threads] = (n, dt, algorithmic_bytes(n, cols, op) / dt / 1e9)
+        res[threads] = (n, dt, algorithmic_bytes(n, cols, op, scale_kind) / dt / 1e9)
     what = "quantize+dequantize" if op != "quantize" else "quantize"
     n1, dt1, gbs1 = res[1]
     n, dt, gbs = res[cores]
@@ -288,7 +294,10 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     w = synth.workload(HEADLINE)
-    x = synth.generate(HEADLINE, device="cuda:0" if torch.cuda.is_available() else "cpu")["x"]
+    # The steps sample rows of a 16384-row instance of the workload's recipe (same row
+    # distribution: the zero and spike rows keep their fractions), so drawing it stays cheap.
+    x = synth.generate(HEADLINE, device="cuda:0" if torch.cuda.is_available() else "cpu",
+                       rows=min(w.rows, 16384))["x"]
     cores = host_cores()
     rows_per_step = 8 * cores
     total_rows = rows_per_step * (args.steps + args.warmup)
@@ -309,11 +318,13 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{w.name} (workload {w.index}) sample", "rows": x.shape[0],
+        "config": {"workload": f"{w.name} (workload {w.index}) sample", "rows": w.rows,
+                   "sampled_from_rows": x.shape[0],
                    "cols": w.cols, "rows_per_step": rows_per_step, "op": "roundtrip",
                    "scale": "row", "mode": "four_over_six"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{rows_per_step} rows of {x.shape[0]}x{w.cols} per step, "
+                         "sample": f"{rows_per_step} evenly spaced rows per step of a "
+                                   f"{x.shape[0]}x{w.cols} draw of the {w.rows}-row recipe, "
                                    f"split over {cores} threads"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -452,7 +463,8 @@ def main():
     x = synth.generate(HEADLINE, device=device)["x"]
     rows, cols = x.shape
 
-    # Headline: fused round trip, timed per launch with events on the launching stream.
+    # Headline: fused round trip on the largest workload, one replay of K captured launches timed
+    # with events on the launching stream.
     with ClockSampler(local) as clocks:
         head = bench_op(nv, x, "roundtrip", "row", "four_over_six", args.steps, args.warmup,
                         world, device)
@@ -480,7 +492,10 @@ def main():
         "frac_of_hbm_peak": round(achieved / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic("fused_roundtrip_row_moe_activation"),
+                     "traffic": recorded_traffic("fused_roundtrip_row_long_rollout"),
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one "
+                                       "launch on this workload (profiles/dram_traffic.txt); "
+                                       "null when the kernel sources changed since",
                      "kernel": "quantize_kernel<four_over_six, row, fused>",
                      "bytes_per_launch": step_bytes, "peak_source": f"{peak_src} hbm_gbs"},
         "gpu_launches": args.steps * head["launches_per_step"],
@@ -495,8 +510,8 @@ def main():
         also = {}
         del x
         torch.cuda.empty_cache()
-        for idx, op, kind, mode in ((3, "quantize", "row", "four_over_six"),
-                                    (4, "roundtrip", "row", "four_over_six"),
+        for idx, op, kind, mode in ((2, "roundtrip", "row", "four_over_six"),
+                                    (3, "quantize", "row", "four_over_six"),
                                     (4, "quantize", "row", "four_over_six"),
                                     (4, "dequantize", "row", "four_over_six"),
                                     (1, "quantize", "tensor", "four_over_six"),
@@ -529,6 +544,22 @@ def main():
             torch.cuda.empty_cache()
         line["also"] = also
         line["device_status_after_extras"] = nv.nvfp4_get_device_status()
+        if rank == 0:
+            # The oracle on a bounded sample of every workload, in the operation that workload
+            # names (about cpu-seconds / 5 of CPU time each).
+            cpus = {}
+            for idx, op, kind, mode in ((0, "roundtrip", "row", "four_over_six"),
+                                        (1, "roundtrip", "tensor", "four_over_six"),
+                                        (2, "roundtrip", "row", "four_over_six"),
+                                        (3, "quantize", "row", "four_over_six"),
+                                        (4, "roundtrip", "row", "four_over_six")):
+                ww = synth.workload(idx)
+                d = synth.generate(idx, device=device)
+                cb = cpu_baseline(d["x"], op, max(1.0, args.cpu_seconds / 5), kind, mode)
+                cpus[f"{ww.name}/{op}/{kind}/{mode}"] = cb
+                del d
+                torch.cuda.empty_cache()
+            line["cpu_baselines"] = cpus
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -248,7 +248,10 @@ nvfp4_status nvfp4_gemm_nt(const uint8_t* x_codes, const uint8_t* x_scales_swizz
                            nvfp4_stream_t stream);
 
 /* Reads (and, if clear != 0, resets to NVFP4_OK) the device status word of the current device.
- * Synchronizes the device.  *status_out receives NVFP4_OK or the first device-side error. */
+ * Synchronizes the device.  *status_out receives NVFP4_OK or the first device-side error.
+ * The library looks up the device addresses of its own device variables (this status word, the
+ * allocation-free call's array) once per device and keeps them for the life of the process, so
+ * it must not be used on a device after cudaDeviceReset or a teardown of its primary context. */
 nvfp4_status nvfp4_get_device_status(int clear, nvfp4_status* status_out);
 
 /* Static, NUL-terminated description of a status code. */
@@ -263,6 +266,17 @@ nvfp4_status nvfp4_set_launch_config(int warps_per_cta, int stages, int max_ctas
  * barrier nothing arrives on, giving up after `timeout_ns` nanoseconds (1 ms default if 0) and
  * recording NVFP4_ERR_TIMEOUT in the device status word.  The wait always ends. */
 nvfp4_status nvfp4_selftest_wait_timeout(uint64_t timeout_ns, nvfp4_stream_t stream);
+
+/* Self-test of the quantize kernels' own failure path.  Until it is called again with row = -1,
+ * every quantize call (row or tensor scale, plain, fused or residual) withholds the
+ * shared-memory copies of row `row` of its input: the warps that own that row wait on their ring
+ * barrier in vain, give up after timeout_ns nanoseconds, record NVFP4_ERR_TIMEOUT in the device
+ * status word, wait (within the library's usual 4 s bound) for their other copies still in
+ * flight, and return, leaving their remaining rows unwritten; warps sharing a row leave together.
+ * Every other wait keeps working, so every launch ends.  timeout_ns must be in (0, 4e9] when
+ * row >= 0; row = -1 restores normal operation (timeout_ns ignored).  Process-wide, for tests
+ * only: do not call it while other threads issue quantize calls. */
+nvfp4_status nvfp4_selftest_withhold_row(int64_t row, uint64_t timeout_ns);
 
 /* ABI version of this header (incremented on incompatible changes). */
 int nvfp4_abi_version(void);

@@ -21,7 +21,8 @@ __all__ = [
     "nvfp4_tensor_amax", "nvfp4_quantize_tensor_noalloc", "nvfp4_dequantize", "nvfp4_fused_roundtrip",
     "nvfp4_swizzled_scales_bytes", "nvfp4_swizzle_block_scales", "nvfp4_gemm_workspace_bytes",
     "nvfp4_gemm_nt", "nvfp4_tensor_workspace_bytes", "nvfp4_get_device_status", "nvfp4_status_string",
-    "nvfp4_set_launch_config", "nvfp4_selftest_wait_timeout", "nvfp4_abi_version", "library",
+    "nvfp4_set_launch_config", "nvfp4_selftest_wait_timeout", "nvfp4_selftest_withhold_row",
+    "nvfp4_abi_version", "library",
 ]
 
 MODE_SIX = 0
@@ -86,6 +87,7 @@ def library():
         "nvfp4_status_string": [I],
         "nvfp4_set_launch_config": [I, I, I],
         "nvfp4_selftest_wait_timeout": [ctypes.c_uint64, P],
+        "nvfp4_selftest_withhold_row": [I64, ctypes.c_uint64],
         "nvfp4_abi_version": [],
     }
     for name, args in sigs.items():
@@ -114,6 +116,14 @@ def _stream(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _on(device, name, *args):
+    """Calls the library's `name` with `device` current: the library finds its per-device state
+    (status word, multiprocessor count, the allocation-free call's array) through the current
+    device, which must be the one that holds the call's tensors."""
+    with torch.cuda.device(device):
+        return getattr(library(), name)(*args)
 
 
 def _need(t, name, dtype, shape, device):
@@ -168,7 +178,7 @@ def nvfp4_quantize_residual(x, mode="four_over_six", stream=None):
                      torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev),
                      torch.empty((rows,), dtype=torch.float32, device=dev)))
     (c, s, d), (rc, rs, rd) = outs
-    st = library().nvfp4_quantize_residual(_ptr(x), rows, cols, _MODES[mode], _ptr(c), _ptr(s),
+    st = _on(dev, "nvfp4_quantize_residual", _ptr(x), rows, cols, _MODES[mode], _ptr(c), _ptr(s),
                                            _ptr(d), _ptr(rc), _ptr(rs), _ptr(rd),
                                            _stream(stream, dev))
     _check(st, "nvfp4_quantize_residual")
@@ -179,8 +189,8 @@ def nvfp4_row_amax(x, row_amax=None, stream=None):
     """Per-token amax, float32 [rows]."""
     rows, cols = _input(x)
     row_amax = _out(row_amax, "row_amax", torch.float32, (rows,), x.device)
-    _check(library().nvfp4_row_amax(_ptr(x), rows, cols, _ptr(row_amax), _stream(stream, x.device)),
-           "nvfp4_row_amax")
+    _check(_on(x.device, "nvfp4_row_amax", _ptr(x), rows, cols, _ptr(row_amax),
+               _stream(stream, x.device)), "nvfp4_row_amax")
     return row_amax
 
 
@@ -193,7 +203,7 @@ def nvfp4_quantize_guided(x, row_amax, ref_codes, ref_block_scales, mode="four_o
     _need(ref_codes, "ref_codes", torch.uint8, (rows, cols // 2), dev)
     _need(ref_block_scales, "ref_block_scales", torch.uint8, (rows, cols // 16), dev)
     codes = _out(codes, "codes", torch.uint8, (rows, cols // 2), dev)
-    st = library().nvfp4_quantize_guided(_ptr(x), rows, cols, _MODES[mode], _ptr(row_amax),
+    st = _on(dev, "nvfp4_quantize_guided", _ptr(x), rows, cols, _MODES[mode], _ptr(row_amax),
                                          _ptr(ref_codes), _ptr(ref_block_scales), _ptr(codes),
                                          _stream(stream, dev))
     _check(st, "nvfp4_quantize_guided")
@@ -211,7 +221,7 @@ def nvfp4_swizzle_block_scales(block_scales, cols, out=None, stream=None):
     _need(block_scales, "block_scales", torch.uint8, (rows, cols // 16), dev)
     n = nvfp4_swizzled_scales_bytes(rows, cols)
     out = _out(out, "out", torch.uint8, (n,), dev)
-    _check(library().nvfp4_swizzle_block_scales(_ptr(block_scales), rows, cols, _ptr(out),
+    _check(_on(dev, "nvfp4_swizzle_block_scales", _ptr(block_scales), rows, cols, _ptr(out),
                                                 _stream(stream, dev)),
            "nvfp4_swizzle_block_scales")
     return out
@@ -231,7 +241,7 @@ def nvfp4_gemm_nt(x_codes, x_scales_swizzled, x_row_scale, w_codes, w_scales_swi
     need = nvfp4_gemm_workspace_bytes(m, n)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    st = library().nvfp4_gemm_nt(_ptr(x_codes), _ptr(x_scales_swizzled), _ptr(x_row_scale),
+    st = _on(dev, "nvfp4_gemm_nt", _ptr(x_codes), _ptr(x_scales_swizzled), _ptr(x_row_scale),
                                  _ptr(w_codes), _ptr(w_scales_swizzled), _ptr(w_tensor_scale),
                                  m, n, k, _ptr(y), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream, dev))
@@ -258,7 +268,7 @@ def nvfp4_quantize_rowwise(x, mode="four_over_six", group_offsets=None, codes=No
             raise ValueError("group_offsets must be 1-D with num_groups + 1 entries")
         _need(group_offsets, "group_offsets", torch.int32, group_offsets.shape, dev)
         groups = group_offsets.numel() - 1
-    st = library().nvfp4_quantize_rowwise(_ptr(x), rows, cols, _ptr(group_offsets), groups,
+    st = _on(dev, "nvfp4_quantize_rowwise", _ptr(x), rows, cols, _ptr(group_offsets), groups,
                                           _MODES[mode], _ptr(codes), _ptr(block_scales),
                                           _ptr(row_scale), _stream(stream, dev))
     _check(st, "nvfp4_quantize_rowwise")
@@ -274,7 +284,7 @@ def nvfp4_quantize_tensor(x, mode="four_over_six", codes=None, block_scales=None
     block_scales = _out(block_scales, "block_scales", torch.uint8, (rows, cols // 16), dev)
     tensor_scale = _out(tensor_scale, "tensor_scale", torch.float32, (1,), dev)
     workspace = _workspace(workspace, dev)
-    st = library().nvfp4_quantize_tensor(_ptr(x), rows, cols, _MODES[mode], _ptr(codes),
+    st = _on(dev, "nvfp4_quantize_tensor", _ptr(x), rows, cols, _MODES[mode], _ptr(codes),
                                          _ptr(block_scales), _ptr(tensor_scale), _ptr(workspace),
                                          workspace.numel() * workspace.element_size(),
                                          _stream(stream, dev))
@@ -289,7 +299,7 @@ def nvfp4_tensor_amax(x, amax=None, workspace=None, stream=None):
     dev = x.device
     amax = _out(amax, "amax", torch.float32, (1,), dev)
     workspace = _workspace(workspace, dev)
-    st = library().nvfp4_tensor_amax(_ptr(x), x.numel(), _ptr(amax), _ptr(workspace),
+    st = _on(dev, "nvfp4_tensor_amax", _ptr(x), x.numel(), _ptr(amax), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(),
                                      _stream(stream, dev))
     _check(st, "nvfp4_tensor_amax")
@@ -305,7 +315,7 @@ def nvfp4_quantize_tensor_with_amax(x, amax, mode="four_over_six", codes=None,
     codes = _out(codes, "codes", torch.uint8, (rows, cols // 2), dev)
     block_scales = _out(block_scales, "block_scales", torch.uint8, (rows, cols // 16), dev)
     tensor_scale = _out(tensor_scale, "tensor_scale", torch.float32, (1,), dev)
-    st = library().nvfp4_quantize_tensor_with_amax(_ptr(x), rows, cols, _MODES[mode], _ptr(amax),
+    st = _on(dev, "nvfp4_quantize_tensor_with_amax", _ptr(x), rows, cols, _MODES[mode], _ptr(amax),
                                                    _ptr(codes), _ptr(block_scales),
                                                    _ptr(tensor_scale), _stream(stream, dev))
     _check(st, "nvfp4_quantize_tensor_with_amax")
@@ -323,7 +333,7 @@ def nvfp4_quantize_tensor_noalloc(x, mode="four_over_six", codes=None, block_sca
     codes = _out(codes, "codes", torch.uint8, (rows, cols // 2), dev)
     block_scales = _out(block_scales, "block_scales", torch.uint8, (rows, cols // 16), dev)
     tensor_scale = _out(tensor_scale, "tensor_scale", torch.float32, (1,), dev)
-    st = library().nvfp4_quantize_tensor_noalloc(_ptr(x), rows, cols, _MODES[mode], _ptr(codes),
+    st = _on(dev, "nvfp4_quantize_tensor_noalloc", _ptr(x), rows, cols, _MODES[mode], _ptr(codes),
                                                  _ptr(block_scales), _ptr(tensor_scale),
                                                  _stream(stream, dev))
     _check(st, "nvfp4_quantize_tensor_noalloc")
@@ -341,7 +351,7 @@ def nvfp4_dequantize(codes, block_scales, scale, kind="row", y=None, stream=None
     k = _KINDS[kind]
     _need(scale, "scale", torch.float32, (rows,) if k == SCALE_ROW else (1,), dev)
     y = _out(y, "y", torch.bfloat16, (rows, cols), dev)
-    st = library().nvfp4_dequantize(_ptr(codes), _ptr(block_scales), _ptr(scale), k, rows, cols,
+    st = _on(dev, "nvfp4_dequantize", _ptr(codes), _ptr(block_scales), _ptr(scale), k, rows, cols,
                                     _ptr(y), _stream(stream, dev))
     _check(st, "nvfp4_dequantize")
     return y
@@ -361,7 +371,7 @@ def nvfp4_fused_roundtrip(x, kind="row", mode="four_over_six", codes=None, block
     if k == SCALE_TENSOR:
         ws = _workspace(workspace, dev)
         ws_bytes = ws.numel() * ws.element_size()
-    st = library().nvfp4_fused_roundtrip(_ptr(x), rows, cols, k, _MODES[mode], _ptr(codes),
+    st = _on(dev, "nvfp4_fused_roundtrip", _ptr(x), rows, cols, k, _MODES[mode], _ptr(codes),
                                          _ptr(block_scales), _ptr(scale), _ptr(y), _ptr(ws),
                                          ws_bytes, _stream(stream, dev))
     _check(st, "nvfp4_fused_roundtrip")
@@ -400,7 +410,7 @@ def nvfp4_fused_roundtrip_host(x, mode="four_over_six", codes=None, block_scales
     need = nvfp4_roundtrip_host_workspace_bytes(cols)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    st = library().nvfp4_fused_roundtrip_host(_ptr(x), rows, cols, _MODES[mode], _ptr(codes),
+    st = _on(dev, "nvfp4_fused_roundtrip_host", _ptr(x), rows, cols, _MODES[mode], _ptr(codes),
                                               _ptr(block_scales), _ptr(row_scale), _ptr(y),
                                               _ptr(workspace),
                                               workspace.numel() * workspace.element_size(),
@@ -428,8 +438,15 @@ def nvfp4_set_launch_config(warps_per_cta=0, stages=0, max_ctas=0):
 
 def nvfp4_selftest_wait_timeout(timeout_ns=1_000_000, stream=None, device=None):
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
-    _check(library().nvfp4_selftest_wait_timeout(timeout_ns, _stream(stream, dev)),
+    _check(_on(dev, "nvfp4_selftest_wait_timeout", timeout_ns, _stream(stream, dev)),
            "nvfp4_selftest_wait_timeout")
+
+
+def nvfp4_selftest_withhold_row(row=-1, timeout_ns=0):
+    """Test hook: quantize calls withhold row `row`'s copies and give up after timeout_ns
+    (row = -1 restores normal operation)."""
+    _check(library().nvfp4_selftest_withhold_row(int(row), int(timeout_ns)),
+           "nvfp4_selftest_withhold_row")
 
 
 def nvfp4_abi_version():

@@ -18,11 +18,12 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // bound on any barrier wait: 4 s
 
 std::atomic<int> g_override_warps{0};
 std::atomic<int> g_override_stages{0};
 std::atomic<int> g_override_max_ctas{0};
+std::atomic<long long> g_withhold_row{-1};        // nvfp4_selftest_withhold_row
+std::atomic<unsigned long long> g_withhold_timeout_ns{0};
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int*> g_status_ptr[kMaxDevices];
 
@@ -98,21 +99,6 @@ nvfp4_status check_workspace(const void* workspace, size_t bytes) {
   return NVFP4_OK;
 }
 
-QuantParams base_params(const void* x, int64_t rows, int64_t cols, uint8_t* codes,
-                        uint8_t* block_scales, float* scale, void* y, int* status) {
-  QuantParams p{};
-  p.x = static_cast<const uint16_t*>(x);
-  p.rows = rows;
-  p.cols = static_cast<int32_t>(cols);
-  p.codes = codes;
-  p.scales = block_scales;
-  p.scale_out = scale;
-  p.y = static_cast<uint16_t*>(y);
-  p.status = status;
-  p.timeout_ns = kWaitTimeoutNs;
-  return p;
-}
-
 // Tensor-scale quantize (optionally fused): amax partials into the workspace, then the encoder.
 nvfp4_status run_tensor(const void* x, int64_t rows, int64_t cols, int mode, uint8_t* codes,
                         uint8_t* block_scales, float* scale, void* y, bool fused, void* workspace,
@@ -125,7 +111,7 @@ nvfp4_status run_tensor(const void* x, int64_t rows, int64_t cols, int mode, uin
   err = launch_amax_partials(static_cast<const uint16_t*>(x), rows * cols, partials, &n_partials,
                              stream);
   if (err != cudaSuccess) return NVFP4_ERR_CUDA;
-  QuantParams p = base_params(x, rows, cols, codes, block_scales, scale, y, status);
+  QuantParams p = make_quant_params(x, rows, cols, codes, block_scales, scale, y, status);
   p.amax_src = partials;
   p.n_amax = n_partials;
   return from_cuda(launch_quantize(mode, true, fused, p, stream, true));
@@ -141,6 +127,24 @@ int check_tensor_quantize_args(const void* x, int64_t rows, int64_t cols, int mo
 }
 
 cudaError_t device_status_word(int** out) { return status_ptr(out); }
+
+QuantParams make_quant_params(const void* x, int64_t rows, int64_t cols, uint8_t* codes,
+                              uint8_t* block_scales, float* scale, void* y, int* status) {
+  QuantParams p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.rows = rows;
+  p.cols = static_cast<int32_t>(cols);
+  p.codes = codes;
+  p.scales = block_scales;
+  p.scale_out = scale;
+  p.y = static_cast<uint16_t*>(y);
+  p.status = status;
+  p.timeout_ns = kWaitTimeoutNs;
+  p.drain_timeout_ns = kWaitTimeoutNs;
+  p.withhold_row = g_withhold_row.load();
+  if (p.withhold_row >= 0) p.timeout_ns = g_withhold_timeout_ns.load();
+  return p;
+}
 
 LaunchOverride launch_override() {
   return {g_override_warps.load(), g_override_stages.load(), g_override_max_ctas.load()};
@@ -174,7 +178,7 @@ nvfp4_status nvfp4_quantize_rowwise(const void* x, int64_t rows, int64_t cols,
   if (st != NVFP4_OK || noop) return st;
   int* status = nullptr;
   if (status_ptr(&status) != cudaSuccess) return NVFP4_ERR_CUDA;
-  QuantParams p = base_params(x, rows, cols, codes, block_scales, row_scale, nullptr, status);
+  QuantParams p = make_quant_params(x, rows, cols, codes, block_scales, row_scale, nullptr, status);
   p.offsets = group_offsets;
   p.num_groups = num_groups;
   return from_cuda(launch_quantize(mode, false, false, p, reinterpret_cast<cudaStream_t>(stream)));
@@ -200,7 +204,7 @@ nvfp4_status nvfp4_quantize_residual(const void* x, int64_t rows, int64_t cols, 
       if (overlap(a[i], an[i], b[j], an[j])) return NVFP4_ERR_INVALID_ARG;
   int* status = nullptr;
   if (status_ptr(&status) != cudaSuccess) return NVFP4_ERR_CUDA;
-  QuantParams p = base_params(x, rows, cols, codes, block_scales, row_scale, nullptr, status);
+  QuantParams p = make_quant_params(x, rows, cols, codes, block_scales, row_scale, nullptr, status);
   p.res_codes = res_codes;
   p.res_scales = res_block_scales;
   p.res_scale_out = res_row_scale;
@@ -285,7 +289,7 @@ nvfp4_status nvfp4_quantize_tensor_with_amax(const void* x, int64_t rows, int64_
   if (!aligned(amax, 4)) return NVFP4_ERR_ALIGNMENT;
   int* status = nullptr;
   if (status_ptr(&status) != cudaSuccess) return NVFP4_ERR_CUDA;
-  QuantParams p = base_params(x, rows, cols, codes, block_scales, tensor_scale, nullptr, status);
+  QuantParams p = make_quant_params(x, rows, cols, codes, block_scales, tensor_scale, nullptr, status);
   p.amax_src = amax;
   p.n_amax = 1;
   return from_cuda(launch_quantize(mode, true, false, p, reinterpret_cast<cudaStream_t>(stream)));
@@ -328,7 +332,7 @@ nvfp4_status nvfp4_fused_roundtrip(const void* x, int64_t rows, int64_t cols,
   }
   int* status = nullptr;
   if (status_ptr(&status) != cudaSuccess) return NVFP4_ERR_CUDA;
-  QuantParams p = base_params(x, rows, cols, codes, block_scales, scale, y, status);
+  QuantParams p = make_quant_params(x, rows, cols, codes, block_scales, scale, y, status);
   return from_cuda(launch_quantize(mode, false, true, p, s));
 }
 
@@ -375,6 +379,14 @@ nvfp4_status nvfp4_selftest_wait_timeout(uint64_t timeout_ns, nvfp4_stream_t str
   if (status_ptr(&status) != cudaSuccess) return NVFP4_ERR_CUDA;
   return from_cuda(launch_wait_timeout_selftest(status, timeout_ns ? timeout_ns : 1000000ull,
                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_selftest_withhold_row(int64_t row, uint64_t timeout_ns) {
+  if (row < -1 || (row >= 0 && (timeout_ns == 0 || timeout_ns > kWaitTimeoutNs)))
+    return NVFP4_ERR_INVALID_ARG;
+  g_withhold_timeout_ns.store(timeout_ns);
+  g_withhold_row.store(row);
+  return NVFP4_OK;
 }
 
 int nvfp4_abi_version(void) { return 1; }

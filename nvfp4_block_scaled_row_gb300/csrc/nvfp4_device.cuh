@@ -66,7 +66,9 @@ struct QuantParams {
   uint32_t slot_bytes;      // bytes per ring slot (>= 32 * blocks_per_warp, multiple of 128)
   int32_t prologue_before_wait;  // 1: the first row copies may precede griddepcontrol.wait
   int* status;              // device status word
-  uint64_t timeout_ns;      // bound on every barrier wait
+  uint64_t timeout_ns;      // bound on every ring-slot wait
+  uint64_t drain_timeout_ns;  // bound on each wait for a copy still in flight before an early exit
+  int64_t withhold_row;     // self-test only: the row whose copies are never issued (-1: none)
 };
 
 struct GuidedParams {
@@ -322,6 +324,30 @@ __device__ __forceinline__ f32x2 fma_f16x2_f32x2(uint32_t a, uint32_t b, f32x2 c
       : "=f"(d0), "=f"(d1)
       : "r"(a), "r"(b), "f"(c0), "f"(c1));
   return pack2(d0, d1);
+}
+
+// Residuals of two elements (2j, 2j+1) under two candidates at once: with a = the first
+// candidate's decoded FP16 pair, b = the second's, and na / nb their negated scales (-s, -s) as
+// FP16 pairs, returns even = (z0 - a.lo*s_a, z0 - b.lo*s_b) and odd = (z1 - a.hi*s_a,
+// z1 - b.hi*s_b), each one FP32 rounding of the exact value (FP16 operands widen exactly).
+__device__ __forceinline__ void residuals_two_candidates(uint32_t a, uint32_t na, uint32_t b,
+                                                         uint32_t nb, f32x2 z, f32x2& even,
+                                                         f32x2& odd) {
+  float z0, z1, ae, be, ao, bo;
+  unpack2(z, z0, z1);
+  asm("{\n\t.reg .f16 a0, a1, b0, b1, sa, sb, xa, xb;\n\t"
+      "mov.b32 {a0, a1}, %4;\n\t"
+      "mov.b32 {b0, b1}, %6;\n\t"
+      "mov.b32 {sa, xa}, %5;\n\t"
+      "mov.b32 {sb, xb}, %7;\n\t"
+      "fma.rn.f32.f16 %0, a0, sa, %8;\n\t"
+      "fma.rn.f32.f16 %1, b0, sb, %8;\n\t"
+      "fma.rn.f32.f16 %2, a1, sa, %9;\n\t"
+      "fma.rn.f32.f16 %3, b1, sb, %9;\n\t}"
+      : "=f"(ae), "=f"(be), "=f"(ao), "=f"(bo)
+      : "r"(a), "r"(na), "r"(b), "r"(nb), "f"(z0), "f"(z1));
+  even = pack2(ae, be);
+  odd = pack2(ao, bo);
 }
 
 // FP32 pair to FP16 pair (RNE): .x to the low half.

@@ -135,16 +135,9 @@ extern "C" nvfp4_status nvfp4_fused_roundtrip_host(const void* x, int64_t rows, 
     if (!check(cudaMemcpyAsync(base + L.x, static_cast<const unsigned char*>(x) + r0 * cols * 2, xb,
                                cudaMemcpyHostToDevice, st)))
       break;
-    nvfp4::QuantParams p{};
-    p.x = reinterpret_cast<const uint16_t*>(base + L.x);
-    p.rows = n;
-    p.cols = static_cast<int32_t>(cols);
-    p.codes = base + L.codes;
-    p.scales = base + L.scales;
-    p.scale_out = reinterpret_cast<float*>(base + L.sdec);
-    p.y = reinterpret_cast<uint16_t*>(base + L.y);
-    p.status = status;
-    p.timeout_ns = 4000000000ull;
+    const nvfp4::QuantParams p = nvfp4::make_quant_params(
+        base + L.x, n, cols, base + L.codes, base + L.scales,
+        reinterpret_cast<float*>(base + L.sdec), base + L.y, status);
     if (!check(nvfp4::launch_quantize(mode, false, true, p, st))) break;
     if (!check(cudaMemcpyAsync(codes + r0 * cols / 2, base + L.codes, cb, cudaMemcpyDeviceToHost,
                                st)) ||

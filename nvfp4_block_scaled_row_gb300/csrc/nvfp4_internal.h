@@ -27,6 +27,14 @@ cudaError_t launch_programmatic(void (*kern)(Params...), dim3 grid, dim3 block, 
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Bound on every device-side barrier wait of the library: 4 s.
+constexpr uint64_t kWaitTimeoutNs = 4000000000ull;
+
+// Quantize parameters with the library's wait bounds (and the withheld-row self-test setting of
+// nvfp4_selftest_withhold_row); the caller fills the mode-specific fields.
+QuantParams make_quant_params(const void* x, int64_t rows, int64_t cols, uint8_t* codes,
+                              uint8_t* block_scales, float* scale, void* y, int* status);
+
 // Launch-shape overrides (0 = automatic), set through nvfp4_set_launch_config.
 struct LaunchOverride {
   int warps_per_cta;

@@ -75,17 +75,10 @@ extern "C" nvfp4_status nvfp4_quantize_tensor_noalloc(const void* x, int64_t row
                                        kNoAllocPartials, &n_partials, &too_small, s);
   if (err != cudaSuccess) return NVFP4_ERR_CUDA;
   if (too_small) return NVFP4_ERR_WORKSPACE;  // more partial maxima than the array holds
-  nvfp4::QuantParams p{};
-  p.x = static_cast<const uint16_t*>(x);
-  p.rows = rows;
-  p.cols = static_cast<int32_t>(cols);
-  p.codes = codes;
-  p.scales = block_scales;
-  p.scale_out = tensor_scale;
+  nvfp4::QuantParams p = nvfp4::make_quant_params(x, rows, cols, codes, block_scales,
+                                                  tensor_scale, nullptr, status);
   p.amax_src = scratch;
   p.n_amax = n_partials;
-  p.status = status;
-  p.timeout_ns = 4000000000ull;
   return nvfp4::launch_quantize(mode, true, false, p, s, true) == cudaSuccess ? NVFP4_OK
                                                                               : NVFP4_ERR_CUDA;
 }

@@ -14,10 +14,10 @@
 //           for both candidates, their block squared errors, the 4/6 choice, and the stores.
 // Each launch is a programmatic dependent of the previous kernel on the stream: shared-memory
 // set-up (and an L2 prefetch of the first rows) overlaps that kernel's tail.
-// Lanes of a quarter-warp read alternate 16-byte halves of their 32-byte blocks first, which
-// keeps every 128-bit shared-memory read free of bank conflicts.  The errors are summed in the
-// fixed order the spec prescribes (four FMA chains, then a pairwise combine), so the result is
-// bit-identical to the CPU oracle and independent of the launch shape.
+// Each block's squared errors are summed in the spec's fixed order -- one FMA chain per
+// candidate over the 16 elements in ascending order, the two candidates' chains side by side in
+// one packed FP32 pair -- so the result is bit-identical to the CPU oracle and independent of the
+// launch shape.
 #include <atomic>
 #include <cfloat>
 
@@ -70,42 +70,54 @@ __device__ __forceinline__ RowFactors row_factors_warp(float a, int lane) {
   return f;
 }
 
-// One candidate (scale-to-6 or scale-to-4) for a block whose targets z are held as 8 FP32
-// pairs (pairs 0-3: half A, pairs 4-7: half B).  Produces the two packed code words, the 8
-// decoded FP16 pairs, and the block squared error
-//   e = (E[A][even] + E[A][odd]) + (E[B][even] + E[B][odd]),
-// each E an FMA chain over every second element of the half, in ascending order.
+// One candidate (scale-to-6 or scale-to-4) for a block whose 16 targets z are held as 8 FP32
+// pairs in element order: the two packed code words (elements 0-7, then 8-15) and the 8 decoded
+// FP16 pairs (element 2j in the low half of r[j]).
+struct Codes {
+  uint32_t cw[2];
+  uint32_t r[8];
+};
+
+__device__ __forceinline__ Codes encode_codes(const f32x2 (&z)[8], float inv) {
+  Codes c;
+  const f32x2 inv2 = pack2(inv, inv);
+  f32x2 t[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) t[j] = mul2(z[j], inv2);  // target scaled down by 1/s
+  uint32_t lo[4], hi[4];
+  c.cw[0] = e2m1x8_encode_decode(t[0], t[1], t[2], t[3], lo);
+  c.cw[1] = e2m1x8_encode_decode(t[4], t[5], t[6], t[7], hi);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    c.r[j] = lo[j];
+    c.r[4 + j] = hi[j];
+  }
+  return c;
+}
+
+// The block squared errors of both candidates ("NVFP4 RL" blog, Sec. 4: the blockwise error in
+// FP32), each summed from +0 over the 16 elements in ascending order, e = fma(d_i, d_i, e), with
+// d_i = z_i - r_i * s one rounding of the exact value (r * s is exact).  The two chains run side
+// by side in one FP32 pair: .x the scale-to-6 error, .y the scale-to-4 error.
+__device__ __forceinline__ f32x2 block_errors(const f32x2 (&z)[8], const Codes& c6, uint32_t ns6,
+                                              const Codes& c4, uint32_t ns4) {
+  f32x2 acc = pack2(0.0f, 0.0f);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    f32x2 even, odd;
+    residuals_two_candidates(c6.r[j], ns6, c4.r[j], ns4, z[j], even, odd);
+    acc = fma2(even, even, acc);  // element 2j
+    acc = fma2(odd, odd, acc);    // element 2j + 1
+  }
+  return acc;
+}
+
+// One candidate with the FP16 selector's error (see encode_candidate_fp16).
 struct Candidate {
   uint32_t cw[2];
   uint32_t r[8];
   float err;
 };
-
-__device__ __forceinline__ Candidate encode_candidate(const f32x2 (&z)[8], const ScaleEntry e) {
-  Candidate c;
-  const f32x2 inv2 = pack2(e.inv, e.inv);
-  f32x2 t[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) t[j] = mul2(z[j], inv2);  // target scaled down by 1/s
-  uint32_t rA[4], rB[4];
-  c.cw[0] = e2m1x8_encode_decode(t[0], t[1], t[2], t[3], rA);
-  c.cw[1] = e2m1x8_encode_decode(t[4], t[5], t[6], t[7], rB);
-  f32x2 accA = pack2(0.0f, 0.0f), accB = pack2(0.0f, 0.0f);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const f32x2 dA = fma_f16x2_f32x2(rA[j], e.neg_s_h2, z[j]);  // z - r*s, one rounding
-    const f32x2 dB = fma_f16x2_f32x2(rB[j], e.neg_s_h2, z[4 + j]);
-    accA = fma2(dA, dA, accA);
-    accB = fma2(dB, dB, accB);
-    c.r[j] = rA[j];
-    c.r[4 + j] = rB[j];
-  }
-  float a0, a1, b0, b1;
-  unpack2(accA, a0, a1);
-  unpack2(accB, b0, b1);
-  c.err = __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(b0, b1));
-  return c;
-}
 
 // The FP16 reading of the 4/6 fast path ("NVFP4 RL" blog, Sec. 4, "The optimization": cast to
 // FP16 losslessly and scale the target down by its inverse): the same targets and codes as
@@ -136,12 +148,12 @@ __device__ __forceinline__ Candidate encode_candidate_fp16(const f32x2 (&z)[8], 
 }
 
 // Encodes one 16-element block with block amax m: both candidates (scale-to-6 only in mode six),
-// the 4/6 choice, then stores the 8 code bytes and the E4M3 scale byte.  Half A holds elements
-// 8*h0 .. 8*h0+7 of the block, half B the other eight.  With kWantY, `out` receives the block's
-// dequantized BF16 pairs (A's four words, then B's) = bf16(fp32(q*s) * S_dec).
+// the 4/6 choice, then stores the 8 code bytes and the E4M3 scale byte.  lo holds elements 0-7
+// of the block, hi elements 8-15.  With kWantY, `out` receives the block's dequantized BF16 pairs
+// in element order = bf16(fp32(q*s) * S_dec).
 template <int kMode, bool kWantY>
-__device__ __forceinline__ void encode_block(const uint4 A, const uint4 B, float m,
-                                             const RowFactors& f, const ScaleEntry* tab, int h0,
+__device__ __forceinline__ void encode_block(const uint4 lo, const uint4 hi, float m,
+                                             const RowFactors& f, const ScaleEntry* tab,
                                              uint8_t* codes_blk, uint8_t* scale_ptr,
                                              uint32_t (&out)[8]) {
   const f32x2 senc2 = pack2(f.S_enc, f.S_enc);
@@ -153,29 +165,44 @@ __device__ __forceinline__ void encode_block(const uint4 A, const uint4 B, float
   const uint32_t b6 = sb & 0xFFu, b4 = sb >> 8;
 
   f32x2 z[8];
-  z[0] = mul2(bf16x2_to_f32x2_fma(A.x, one_bf16, neg_zero), senc2);
-  z[1] = mul2(bf16x2_to_f32x2_fma(A.y, one_bf16, neg_zero), senc2);
-  z[2] = mul2(bf16x2_to_f32x2_fma(A.z, one_bf16, neg_zero), senc2);
-  z[3] = mul2(bf16x2_to_f32x2_fma(A.w, one_bf16, neg_zero), senc2);
-  z[4] = mul2(bf16x2_to_f32x2_fma(B.x, one_bf16, neg_zero), senc2);
-  z[5] = mul2(bf16x2_to_f32x2_fma(B.y, one_bf16, neg_zero), senc2);
-  z[6] = mul2(bf16x2_to_f32x2_fma(B.z, one_bf16, neg_zero), senc2);
-  z[7] = mul2(bf16x2_to_f32x2_fma(B.w, one_bf16, neg_zero), senc2);
+  z[0] = mul2(bf16x2_to_f32x2_fma(lo.x, one_bf16, neg_zero), senc2);
+  z[1] = mul2(bf16x2_to_f32x2_fma(lo.y, one_bf16, neg_zero), senc2);
+  z[2] = mul2(bf16x2_to_f32x2_fma(lo.z, one_bf16, neg_zero), senc2);
+  z[3] = mul2(bf16x2_to_f32x2_fma(lo.w, one_bf16, neg_zero), senc2);
+  z[4] = mul2(bf16x2_to_f32x2_fma(hi.x, one_bf16, neg_zero), senc2);
+  z[5] = mul2(bf16x2_to_f32x2_fma(hi.y, one_bf16, neg_zero), senc2);
+  z[6] = mul2(bf16x2_to_f32x2_fma(hi.z, one_bf16, neg_zero), senc2);
+  z[7] = mul2(bf16x2_to_f32x2_fma(hi.w, one_bf16, neg_zero), senc2);
 
   const ScaleEntry e6 = tab[b6];
-  const Candidate c6 =
-      (kMode == kModeFourOverSixFp16) ? encode_candidate_fp16(z, e6) : encode_candidate(z, e6);
   bool pick4 = false;
-  Candidate c4{};
   ScaleEntry e4{};
-  if (kMode != kModeSix) {
+  uint32_t w0, w1;          // the chosen code words
+  const uint32_t* r;        // the chosen decoded pairs
+  Codes c6, c4;
+  Candidate h6, h4;
+  if (kMode == kModeFourOverSixFp16) {
     e4 = tab[b4];
-    c4 = (kMode == kModeFourOverSixFp16) ? encode_candidate_fp16(z, e4) : encode_candidate(z, e4);
-    pick4 = c4.err < c6.err;  // ties go to 6
+    h6 = encode_candidate_fp16(z, e6);
+    h4 = encode_candidate_fp16(z, e4);
+    pick4 = h4.err < h6.err;  // ties go to 6
+    w0 = pick4 ? h4.cw[0] : h6.cw[0];
+    w1 = pick4 ? h4.cw[1] : h6.cw[1];
+    r = pick4 ? h4.r : h6.r;
+  } else {
+    c6 = encode_codes(z, e6.inv);
+    if (kMode == kModeFourOverSix) {
+      e4 = tab[b4];
+      c4 = encode_codes(z, e4.inv);
+      float err6, err4;
+      unpack2(block_errors(z, c6, e6.neg_s_h2, c4, e4.neg_s_h2), err6, err4);
+      pick4 = err4 < err6;  // ties go to 6
+    }
+    w0 = pick4 ? c4.cw[0] : c6.cw[0];
+    w1 = pick4 ? c4.cw[1] : c6.cw[1];
+    r = pick4 ? c4.r : c6.r;
   }
-  uint32_t* cw = reinterpret_cast<uint32_t*>(codes_blk);
-  cw[h0] = pick4 ? c4.cw[0] : c6.cw[0];
-  cw[1 - h0] = pick4 ? c4.cw[1] : c6.cw[1];
+  *reinterpret_cast<uint2*>(codes_blk) = make_uint2(w0, w1);
   *scale_ptr = static_cast<uint8_t>(pick4 ? b4 : b6);
 
   if (kWantY) {
@@ -184,10 +211,29 @@ __device__ __forceinline__ void encode_block(const uint4 A, const uint4 B, float
     const f32x2 nzero = pack2(-0.0f, -0.0f);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint32_t r = pick4 ? c4.r[j] : c6.r[j];
-      const f32x2 qs = fma_f16x2_f32x2(r, s_h2, nzero);  // q*s, exact
+      const f32x2 qs = fma_f16x2_f32x2(r[j], s_h2, nzero);  // q*s, exact
       out[j] = bf16x2_from_f32x2(mul2(qs, sdec2));
     }
+  }
+}
+
+// A block's two 16-byte halves in element order (lo = elements 0-7) from shared memory.
+// kSwizzled: lanes of a quarter-warp read alternate halves first, so every 128-bit read is free
+// of bank conflicts, and the halves are then put back in element order with selects; otherwise
+// both reads are in element order (two-way bank conflicts, eight fewer instructions per block).
+// Measured: the fused round trip, whose global stores share the memory pipe with these reads, is
+// 2.5% faster swizzled; the issue-bound quantize-only kernels are 5% faster in element order.
+template <bool kSwizzled>
+__device__ __forceinline__ void load_block(const unsigned char* blk, uint4& lo, uint4& hi) {
+  if (kSwizzled) {
+    const int h0 = (threadIdx.x >> 2) & 1;
+    const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
+    const uint4 B = *reinterpret_cast<const uint4*>(blk + (h0 ^ 1) * 16);
+    lo = make_uint4(h0 ? B.x : A.x, h0 ? B.y : A.y, h0 ? B.z : A.z, h0 ? B.w : A.w);
+    hi = make_uint4(h0 ? A.x : B.x, h0 ? A.y : B.y, h0 ? A.z : B.z, h0 ? A.w : B.w);
+  } else {
+    lo = *reinterpret_cast<const uint4*>(blk);
+    hi = *reinterpret_cast<const uint4*>(blk + 16);
   }
 }
 
@@ -303,13 +349,24 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
   const uint64_t policy = l2_evict_first_policy();
   const int h0 = (lane >> 2) & 1;  // which 16-byte half of its block this lane reads first
 
-  // Prologue: fill the ring with this warp's part of the team's first rows.
+  // Prologue: fill the ring with this warp's part of the team's first rows.  (The self-test's
+  // withheld row is never copied, so its slot's barrier never completes.)
   int64_t issued = 0;
   auto issue = [&](int slot_index, int64_t row) {
-    mbar_arrive_expect_tx(&my_bars[slot_index], chunk_bytes);
-    bulk_load(my_ring + static_cast<size_t>(slot_index) * p.slot_bytes, p.x + row * cols + b0 * 16,
-              chunk_bytes, &my_bars[slot_index], policy);
+    if (row != p.withhold_row) {
+      mbar_arrive_expect_tx(&my_bars[slot_index], chunk_bytes);
+      bulk_load(my_ring + static_cast<size_t>(slot_index) * p.slot_bytes,
+                p.x + row * cols + b0 * 16, chunk_bytes, &my_bars[slot_index], policy);
+    }
     ++issued;
+  };
+  // Before an early exit: wait (bounded) for this warp's copies still in flight, those of the
+  // ring steps k, k+1, ..., so that none lands after the warp is gone.
+  auto drain = [&](int64_t k) {
+    for (int64_t i = k; i < issued; ++i)
+      if (gt + i * NT != p.withhold_row)
+        (void)mbar_wait_bounded(&my_bars[i % S], static_cast<uint32_t>((i / S) & 1),
+                                p.drain_timeout_ns);
   };
   if (lane == 0 && has_work)
     for (int s = 0; s < S && gt + s * NT < p.rows; ++s) issue(s, gt + s * NT);
@@ -337,12 +394,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
     const bool team_sync = !kTensor && TW > 1;
     if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
     if (!ok && !team_sync) {
-      // A copy did not land in time: give the copies still in flight one more bounded wait so
-      // none lands after this warp is gone, and stop.
-      if (lane == 0)
-        for (int64_t i = k; i < issued; ++i)
-          (void)mbar_wait_bounded(&my_bars[i % S], static_cast<uint32_t>((i / S) & 1),
-                                  p.timeout_ns);
+      // A copy did not land in time: wait for the copies still in flight, and stop.
+      if (lane == 0) drain(k);
       return;
     }
     unsigned char* xs = my_ring + static_cast<size_t>(slot) * p.slot_bytes;
@@ -374,10 +427,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
         }
         named_barrier(1 + team, TW * 32);
         if (abort_flag[team]) {
-          if (lane == 0)
-            for (int64_t i = k; i < issued; ++i)
-              (void)mbar_wait_bounded(&my_bars[i % S], static_cast<uint32_t>((i / S) & 1),
-                                      p.timeout_ns);
+          if (lane == 0) drain(k);
           return;
         }
         a = 0.0f;
@@ -419,25 +469,25 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
       const int b = b0 + lane + 32 * j;
       if ((kNB == 0 || kResidual) && b >= b1) break;
       unsigned char* blk = xs + (b - b0) * 32;
-      const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
-      const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
-      const float m = abs_max_word(kTensor ? block_max_word(A, B) : bmax[j]);
+      uint4 lo, hi;
+      load_block<kFused>(blk, lo, hi);
+      const float m = abs_max_word(kTensor ? block_max_word(lo, hi) : bmax[j]);
       uint32_t out[8];
-      encode_block<kMode, kFused || kResidual>(A, B, m, f, tab, h0, codes_row + b * 8,
+      encode_block<kMode, kFused || kResidual>(lo, hi, m, f, tab, codes_row + b * 8,
                                                scales_row + b, out);
       if (kFused) {
         uint16_t* y_blk = p.y + row * cols + b * kBlockElems;
-        *reinterpret_cast<uint4*>(y_blk + h0 * 8) = make_uint4(out[0], out[1], out[2], out[3]);
-        *reinterpret_cast<uint4*>(y_blk + (1 - h0) * 8) = make_uint4(out[4], out[5], out[6], out[7]);
+        *reinterpret_cast<uint4*>(y_blk) = make_uint4(out[0], out[1], out[2], out[3]);
+        *reinterpret_cast<uint4*>(y_blk + 8) = make_uint4(out[4], out[5], out[6], out[7]);
       }
       if (kResidual) {
-        const uint4 RA = make_uint4(bf16x2_residual(A.x, out[0]), bf16x2_residual(A.y, out[1]),
-                                    bf16x2_residual(A.z, out[2]), bf16x2_residual(A.w, out[3]));
-        const uint4 RB = make_uint4(bf16x2_residual(B.x, out[4]), bf16x2_residual(B.y, out[5]),
-                                    bf16x2_residual(B.z, out[6]), bf16x2_residual(B.w, out[7]));
-        *reinterpret_cast<uint4*>(blk + h0 * 16) = RA;
-        *reinterpret_cast<uint4*>(blk + (1 - h0) * 16) = RB;
-        rmax[j] = block_max_word(RA, RB);
+        const uint4 RL = make_uint4(bf16x2_residual(lo.x, out[0]), bf16x2_residual(lo.y, out[1]),
+                                    bf16x2_residual(lo.z, out[2]), bf16x2_residual(lo.w, out[3]));
+        const uint4 RH = make_uint4(bf16x2_residual(hi.x, out[4]), bf16x2_residual(hi.y, out[5]),
+                                    bf16x2_residual(hi.z, out[6]), bf16x2_residual(hi.w, out[7]));
+        *reinterpret_cast<uint4*>(blk) = RL;
+        *reinterpret_cast<uint4*>(blk + 16) = RH;
+        rmax[j] = block_max_word(RL, RH);
         rm2 = max_abs_bf16x2(rm2, rmax[j]);
       }
     }
@@ -463,11 +513,10 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
       for (int j = 0; j < (kNB > 0 ? kNB : kMaxBlocksPerLane); ++j) {
         const int b = b0 + lane + 32 * j;
         if (kNB == 0 && b >= b1) break;
-        const unsigned char* blk = xs + (b - b0) * 32;
-        const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
-        const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
+        uint4 lo, hi;
+        load_block<false>(xs + (b - b0) * 32, lo, hi);
         uint32_t unused[8];
-        encode_block<kMode, false>(A, B, abs_max_word(rmax[j]), g, tab, h0, rcodes_row + b * 8,
+        encode_block<kMode, false>(lo, hi, abs_max_word(rmax[j]), g, tab, rcodes_row + b * 8,
                                    rscales_row + b, unused);
       }
       fence_proxy_async_smem();  // the residual writes above precede the slot's next bulk copy

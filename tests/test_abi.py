@@ -169,3 +169,11 @@ def test_host_roundtrip_validation(lib):
     assert f(P(1 << 20), 0, 7168, 1, None, None, None, None, None, 0, None) == OK
     assert f(None, 4, 7168, 1, P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20), P(6 << 20), ws,
              None) == INVALID
+
+
+def test_withhold_row_hook_validation(lib):
+    h = lib.nvfp4_selftest_withhold_row
+    assert h(-2, 1000) == INVALID
+    assert h(3, 0) == INVALID
+    assert h(3, 4_000_000_001) == INVALID
+    assert h(-1, 0) == OK  # normal operation

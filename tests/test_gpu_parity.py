@@ -195,6 +195,23 @@ def test_edge_values_and_ragged_widths(cols):
     check_tensor(x[: min(rows, 9)].contiguous(), F4)
 
 
+def test_block_error_order_blocks():
+    """The two blocks whose 4/6 choice only the ascending order of the error chain decides
+    (test_oracle_method.chain_order_row), tiled along a 7168-wide row so every lane of a team sees
+    them, and alone in a 32-wide row."""
+    from test_oracle_method import chain_order_row
+
+    pair = chain_order_row()[0]
+    wide = np.tile(pair, 7168 // 32)[None, :]
+    for bits in (pair[None, :], wide, np.repeat(wide, 5, axis=0)):
+        x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+        check_rowwise(x)
+        check_tensor(x, F4)
+    codes, scales, _ = nv.nvfp4_quantize_rowwise(
+        torch.from_numpy(pair[None, :].view(np.int16)).view(torch.bfloat16).to(DEV))
+    assert list(_np(scales)[0]) == [0x78, 0x7C]
+
+
 @pytest.mark.parametrize("rows", [1, 2, 7, 31, 33])
 def test_few_rows(rows):
     check_rowwise(_edge_matrix(rows, 7168, seed=rows))
@@ -275,6 +292,41 @@ def test_bounded_wait_reports_timeout():
     assert nv.nvfp4_get_device_status() == 5
     # The context is still healthy afterwards.
     check_rowwise(synth.generate(0, device=DEV, rows=16)["x"])
+
+
+@pytest.mark.parametrize("cols,op", [(7168, "rowwise"), (7168, "fused"), (7168, "tensor"),
+                                     (7168, "residual"), (2048, "rowwise"), (32768, "rowwise")])
+def test_quantize_ring_timeout_path(cols, op):
+    """The quantize kernel's own failure branches: with one row's copies withheld, the warps that
+    own it give up after 1 ms, record NVFP4_ERR_TIMEOUT, drain their copies still in flight and
+    return (a team of several warps -- 2 for 7168-wide rows, 8 for 32768 -- leaves together behind
+    its barrier); the next ordinary call on the same context is bit-exact."""
+    if cols == 2048:
+        x = synth.generate(0, device=DEV, rows=96)["x"]
+    elif cols == 7168:
+        x = synth.generate(2, device=DEV, rows=96)["x"]
+    else:
+        x = _edge_matrix(12, cols, seed=5)
+    nv.nvfp4_get_device_status(clear=True)
+    nv.nvfp4_selftest_withhold_row(3, 1_000_000)
+    try:
+        if op == "rowwise":
+            nv.nvfp4_quantize_rowwise(x)
+        elif op == "fused":
+            nv.nvfp4_fused_roundtrip(x, "row")
+        elif op == "tensor":
+            nv.nvfp4_quantize_tensor(x)
+        else:
+            nv.nvfp4_quantize_residual(x)
+        torch.cuda.synchronize()
+    finally:
+        nv.nvfp4_selftest_withhold_row(-1, 0)
+    assert nv.nvfp4_get_device_status(clear=True) == 5  # NVFP4_ERR_TIMEOUT
+    check_rowwise(x, F4, fused=True, dequant=False)
+    if op == "tensor":
+        check_tensor(x, F4)
+    if op == "residual":
+        check_residual(x)
 
 
 def test_host_validation_errors():
@@ -406,19 +458,26 @@ def _perturbed(x, seed):
     return (x.float() * (1 + noise)).to(torch.bfloat16)
 
 
+def _oracle_record(x_roll):
+    """The rollout's record as the oracle computes it: per-token amax, codes and block scales
+    (numpy, for the oracle) and the same arrays on the device (for the library)."""
+    xb = synth.as_u16(x_roll)
+    amax = np.array([oracle.amax(xb[r]) for r in range(xb.shape[0])], np.float32)
+    q = oracle.quantize(xb, oracle.MODE_FOUR_OVER_SIX, oracle.SCALE_ROW)
+    host = (amax, q["codes"], q["scales"])
+    return host, tuple(torch.from_numpy(a).to(DEV) for a in host)
+
+
 @pytest.mark.parametrize("index,rows", [(0, None), (2, 256), (4, 300)])
 def test_guided_rounding_matches_oracle(index, rows):
     x_roll = synth.generate(index, device=DEV, rows=rows)["x"]
-    amax = nv.nvfp4_row_amax(x_roll)
-    xb = synth.as_u16(x_roll)
-    assert np.array_equal(_np(amax), np.array([oracle.amax(xb[r]) for r in range(xb.shape[0])],
-                                              np.float32))
-    codes, scales, _ = nv.nvfp4_quantize_rowwise(x_roll)
+    (amax_h, codes_h, scales_h), (amax, codes, scales) = _oracle_record(x_roll)
+    _assert_equal(_np(nv.nvfp4_row_amax(x_roll)), amax_h, "row amax")
     same = nv.nvfp4_quantize_guided(x_roll, amax, codes, scales)
     assert torch.equal(same, codes)  # trainer == rollout -> the rollout's codes
     x_tr = _perturbed(x_roll, index)
     got = nv.nvfp4_quantize_guided(x_tr, amax, codes, scales)
-    want = oracle.quantize_guided(synth.as_u16(x_tr), _np(amax), _np(codes), _np(scales))
+    want = oracle.quantize_guided(synth.as_u16(x_tr), amax_h, codes_h, scales_h)
     _assert_equal(_np(got), want, "guided codes")
     own = nv.nvfp4_quantize_guided(x_tr, amax, got, scales)  # idempotent on its own output
     assert torch.equal(own, got)
@@ -428,11 +487,10 @@ def test_guided_rounding_matches_oracle(index, rows):
 @pytest.mark.parametrize("cols", [16, 48, 7184])
 def test_guided_rounding_edge_values(cols):
     x_roll = _edge_matrix(16, cols, seed=cols + 3)
-    amax = nv.nvfp4_row_amax(x_roll)
-    codes, scales, _ = nv.nvfp4_quantize_rowwise(x_roll)
+    (amax_h, codes_h, scales_h), (amax, codes, scales) = _oracle_record(x_roll)
     x_tr = _perturbed(x_roll, cols)
     got = nv.nvfp4_quantize_guided(x_tr, amax, codes, scales)
-    want = oracle.quantize_guided(synth.as_u16(x_tr), _np(amax), _np(codes), _np(scales))
+    want = oracle.quantize_guided(synth.as_u16(x_tr), amax_h, codes_h, scales_h)
     _assert_equal(_np(got), want, "guided codes (edge)")
 
 

@@ -40,11 +40,14 @@ def _noalloc(lib, x, mode):
     return codes, scales, ts
 
 
-@pytest.mark.parametrize("mode", [1, 0])
+@pytest.mark.parametrize("mode", [1, 0, 2])
 def test_noalloc_matches_workspace_entry_point(lib, mode):
-    name = "four_over_six" if mode == 1 else "six"
+    name = {0: "six", 1: "four_over_six", 2: "four_over_six_fp16"}[mode]
+    # The last input is one 4x2048 tensor: its amax pass writes fewer partial maxima than the
+    # calls before it left in the shared array, so a read past them would change its result.
     inputs = [synth.generate(1, device=DEV)["x"],                 # weights, amax ~0.4
-              synth.generate(4, device=DEV, rows=1024)["x"]]       # spikes, amax 3e4
+              synth.generate(4, device=DEV, rows=1024)["x"],       # spikes, amax 3e4
+              synth.generate(0, device=DEV, rows=4)["x"]]          # tiny: one partial maximum
     for x in inputs:
         want = nv.nvfp4_quantize_tensor(x, name)
         torch.cuda.synchronize()
