@@ -227,20 +227,22 @@ size_t nvfp4_swizzled_scales_bytes(int64_t rows, int64_t cols);
 nvfp4_status nvfp4_swizzle_block_scales(const uint8_t* block_scales, int64_t rows, int64_t cols,
                                         uint8_t* swizzled, nvfp4_stream_t stream);
 
-/* Device workspace nvfp4_gemm_nt needs for an m x n product (library GEMM scratch plus the FP32
- * accumulator). */
+/* Scratch bytes nvfp4_gemm_nt needs: 0 (kept so callers that size a workspace keep working). */
 size_t nvfp4_gemm_workspace_bytes(int64_t m, int64_t n);
 
 /* The forward the quantized tensors feed ("NVFP4 RL" Sec. 3: y = x . Q(w); Sec. 2: x with per-token
  * FP32 scales): y[m][n] = bf16(fp32(fp32(D[m][n] * x_row_scale[m]) * w_tensor_scale[0])) with
  * D[m][n] = sum_k (qx[m][k] * sx[m][k/16]) * (qw[n][k] * sw[n][k/16]) accumulated in FP32 on the
- * tensor cores (NVFP4 x NVFP4 block-scaled product, the library's GEMM), then one epilogue pass.
+ * tensor cores: one hand-written kernel (block-scaled FP4 tcgen05 products, the scales applied in
+ * its epilogue; no library GEMM and no FP32 intermediate in memory).
  *   x_codes [m][k/2], w_codes [n][k/2]   E2M1 codes as the quantizer writes them (256-byte aligned)
  *   x_scales_swizzled, w_scales_swizzled block scales in the layout of nvfp4_swizzle_block_scales
+ *                                        (256-byte aligned)
  *   x_row_scale [m], w_tensor_scale [1]  the quantizer's S_dec values
- *   y [m][n] BF16 (16-byte aligned); workspace >= nvfp4_gemm_workspace_bytes(m, n), 256-aligned.
- * k must be a positive multiple of 64 and n of 16.  Not bit-reproducible across libraries: the
- * FP32 accumulation order is the library's. */
+ *   y [m][n] BF16 (16-byte aligned).  workspace / workspace_bytes are unused (may be NULL / 0).
+ * k must be a positive multiple of 64 and n of 16; m, n, k below 2^31 - 256.  Not bit-reproducible
+ * against other GEMMs: the FP32 accumulation order is the tensor core's.  A bounded wait inside
+ * the kernel that runs out records NVFP4_ERR_TIMEOUT in the device status word. */
 nvfp4_status nvfp4_gemm_nt(const uint8_t* x_codes, const uint8_t* x_scales_swizzled,
                            const float* x_row_scale, const uint8_t* w_codes,
                            const uint8_t* w_scales_swizzled, const float* w_tensor_scale, int64_t m,

@@ -232,19 +232,15 @@ def nvfp4_gemm_workspace_bytes(m, n):
 
 
 def nvfp4_gemm_nt(x_codes, x_scales_swizzled, x_row_scale, w_codes, w_scales_swizzled,
-                  w_tensor_scale, y=None, workspace=None, stream=None):
+                  w_tensor_scale, y=None, stream=None):
     """y[m, n] = x . w^T from NVFP4 operands (per-token x scale, per-tensor w scale), BF16."""
     m, k = x_codes.shape[0], x_codes.shape[1] * 2
     n = w_codes.shape[0]
     dev = x_codes.device
     y = _out(y, "y", torch.bfloat16, (m, n), dev)
-    need = nvfp4_gemm_workspace_bytes(m, n)
-    if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     st = _on(dev, "nvfp4_gemm_nt", _ptr(x_codes), _ptr(x_scales_swizzled), _ptr(x_row_scale),
-                                 _ptr(w_codes), _ptr(w_scales_swizzled), _ptr(w_tensor_scale),
-                                 m, n, k, _ptr(y), _ptr(workspace),
-                                 workspace.numel() * workspace.element_size(), _stream(stream, dev))
+             _ptr(w_codes), _ptr(w_scales_swizzled), _ptr(w_tensor_scale), m, n, k, _ptr(y),
+             None, 0, _stream(stream, dev))
     _check(st, "nvfp4_gemm_nt")
     return y
 

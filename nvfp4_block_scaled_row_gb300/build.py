@@ -62,9 +62,7 @@ def build(force=False, verbose=False, extra=()):
         logs = list(ex.map(run, cmds))
     objs = [c[-1] for c in cmds]
     tmp = LIBRARY + ".tmp"
-    cuda_lib = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
-    link = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-L", cuda_lib, "-lcublasLt",
-            "-Xlinker", "-rpath=" + cuda_lib]
+    link = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + " ".join(link) + "\n" + r.stdout + r.stderr)

@@ -38,9 +38,10 @@ def test_exports_match_header(lib):
         assert hasattr(lib, name)
 
 
-def test_no_link_time_dependency_on_the_driver():
+def test_no_link_time_dependency_on_the_driver_or_a_library_gemm():
     out = subprocess.run(["ldd", nvbuild.LIBRARY], capture_output=True, text=True).stdout
     assert "libcuda.so" not in out
+    assert "cublas" not in out.lower()
 
 
 def test_status_strings(lib):
@@ -125,12 +126,17 @@ def test_swizzle_and_gemm_host_validation(lib):
     assert sw(P(1 << 20), 4, 64, P((2 << 20) + 8), None) == ALIGN  # 16-byte lines
     assert sw(P(1 << 20), 4, 64, P(1 << 20), None) == INVALID  # overlaps the input
     g = lib.nvfp4_gemm_nt
-    ws = lib.nvfp4_gemm_workspace_bytes(256, 256)
+    assert lib.nvfp4_gemm_workspace_bytes(256, 256) == 0  # no scratch memory
     ok = [P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20), P(6 << 20)]
-    assert g(*ok, 256, 256, 96, P(7 << 20), P(8 << 20), ws, None) == SHAPE  # k % 64
-    assert g(*ok, 256, 250, 128, P(7 << 20), P(8 << 20), ws, None) == SHAPE  # n % 16
-    assert g(*ok, 256, 256, 128, P((7 << 20) + 8), P(8 << 20), ws, None) == ALIGN
-    assert g(*ok, 256, 256, 128, P(7 << 20), P(8 << 20), ws - 1, None) == WORKSPACE
+    assert g(*ok, 256, 256, 96, P(7 << 20), None, 0, None) == SHAPE  # k % 64
+    assert g(*ok, 256, 250, 128, P(7 << 20), None, 0, None) == SHAPE  # n % 16
+    assert g(*ok, -1, 256, 128, P(7 << 20), None, 0, None) == INVALID
+    assert g(*ok, 0, 256, 128, P(7 << 20), None, 0, None) == OK
+    assert g(*ok, 256, 256, 128, P((7 << 20) + 8), None, 0, None) == ALIGN  # y
+    bad_scale = [ok[0], ok[1], P((3 << 20) + 2)] + ok[3:]
+    assert g(*bad_scale, 256, 256, 128, P(7 << 20), None, 0, None) == ALIGN  # row scale
+    bad_codes = [P((1 << 20) + 128)] + ok[1:]
+    assert g(*bad_codes, 256, 256, 128, P(7 << 20), None, 0, None) == ALIGN  # TMA base
 
 
 def test_launch_config_validation(lib):

@@ -533,30 +533,65 @@ def test_swizzle_block_scales(rows, cols):
     assert np.array_equal(_np(got), _swizzle_reference(_np(scales)))
 
 
-@pytest.mark.parametrize("m,n,k", [(256, 256, 2048), (512, 384, 7168)])
+def _oracle_operand(x, kind):
+    """An operand quantized by the oracle (4/6; per-token for x, per-tensor for w): its host
+    arrays for the float64 reference and the same arrays on the device for the library."""
+    q = oracle.quantize(synth.as_u16(x), oracle.MODE_FOUR_OVER_SIX,
+                        oracle.SCALE_ROW if kind == "row" else oracle.SCALE_TENSOR)
+    return q, tuple(torch.from_numpy(q[k]).to(DEV) for k in ("codes", "scales", "scale"))
+
+
+def _gemm_check(got, X, W, k):
+    """got (float64) against the float64 product X . W^T of the exactly dequantized operands:
+    within the BF16 output rounding (2^-9, plus the two FP32 epilogue roundings) and the FP32
+    accumulation over k terms (at most k * 2^-24 of the magnitude sum)."""
+    ref = X @ W.T
+    mag = np.abs(X) @ np.abs(W).T
+    bound = 2.0 ** -8 * np.abs(ref) + k * 2.0 ** -24 * mag + 1e-30
+    bad = np.abs(got - ref) > bound
+    worst = (np.abs(got - ref) / (np.abs(ref) + k * 2.0 ** -24 * mag + 1e-30)).max()
+    assert not bad.any(), (f"{bad.sum()} of {bad.size} outputs off; first at "
+                           f"{tuple(np.argwhere(bad)[0])}; worst relative error {worst:.3e}")
+    return worst
+
+
+@pytest.mark.parametrize("m,n,k", [(128, 128, 256), (256, 256, 2048), (300, 144, 320),
+                                   (512, 384, 7168)])
 def test_gemm_nt_matches_float64_product(m, n, k):
     """y = x . Q(w) on the tensor cores against the float64 product of the exactly dequantized
-    operands (decoded independently of the library), within FP32-accumulation error."""
+    operands (decoded independently of the library).  Both operands are quantized by the oracle;
+    the shapes cover one tile, ragged row and column tiles and a K that ends mid-stage."""
     from indep import exact_dequant
 
     x = synth.generate(2, device=DEV, rows=m)["x"][:, :k].contiguous()
     w = synth.generate(1, device=DEV, rows=n)["x"][:, :k].contiguous()
-    xc, xs, xd = nv.nvfp4_quantize_rowwise(x)
-    wc, ws, wd = nv.nvfp4_quantize_tensor(w)
+    qx, (xc, xs, xd) = _oracle_operand(x, "row")
+    qw, (wc, ws, wd) = _oracle_operand(w, "tensor")
     y = nv.nvfp4_gemm_nt(xc, nv.nvfp4_swizzle_block_scales(xs, k), xd,
                          wc, nv.nvfp4_swizzle_block_scales(ws, k), wd)
-    X = exact_dequant({"codes": _np(xc), "scales": _np(xs), "scale": _np(xd)}, k)
-    W = exact_dequant({"codes": _np(wc), "scales": _np(ws), "scale": _np(wd)}, k)
-    ref = X @ W.T
-    mag = np.abs(X) @ np.abs(W).T
-    got = y.float().cpu().numpy().astype(np.float64)
-    # BF16 output rounding (2^-9, plus the two FP32 epilogue roundings) and FP32 accumulation over
-    # k terms (at most k * 2^-24 of the magnitude sum; 7168 * 2^-24 = 4.3e-4).
-    bound = 2.0 ** -8 * np.abs(ref) + k * 2.0 ** -24 * mag + 1e-30
-    print(f"gemm {m}x{n}x{k}: max |err| / (|ref| + k 2^-24 mag) = "
-          f"{(np.abs(got - ref) / (np.abs(ref) + k * 2.0 ** -24 * mag + 1e-30)).max():.3e}")
-    bad = np.abs(got - ref) > bound
-    assert not bad.any(), f"{bad.sum()} of {bad.size} outputs off; worst {np.abs(got - ref)[bad].max()}"
+    worst = _gemm_check(y.float().cpu().numpy().astype(np.float64), exact_dequant(qx, k),
+                        exact_dequant(qw, k), k)
+    print(f"gemm {m}x{n}x{k}: worst relative error {worst:.3e}")
+    assert nv.nvfp4_get_device_status() == 0
+
+
+def test_gemm_nt_full_size_sampled_rows():
+    """The benchmark's product, 16384 x 2048 x 7168 (MoE activations times one expert's weight),
+    in its launch configuration; 64 sampled rows of y against the float64 product."""
+    from indep import exact_dequant
+
+    k = 7168
+    x = synth.generate(2, device=DEV)["x"]
+    w = synth.generate(1, device=DEV)["x"]
+    qw, (wc, ws, wd) = _oracle_operand(w, "tensor")
+    xc, xs, xd = nv.nvfp4_quantize_rowwise(x)
+    y = nv.nvfp4_gemm_nt(xc, nv.nvfp4_swizzle_block_scales(xs, k), xd,
+                         wc, nv.nvfp4_swizzle_block_scales(ws, k), wd)
+    rows = _sample_rows(x.shape[0], n=62, seed=3)
+    qx = oracle.quantize(synth.as_u16(x[torch.as_tensor(rows, device=DEV)]),
+                         oracle.MODE_FOUR_OVER_SIX, oracle.SCALE_ROW)
+    got = y[torch.as_tensor(rows, device=DEV)].float().cpu().numpy().astype(np.float64)
+    _gemm_check(got, exact_dequant(qx, k), exact_dequant(qw, k), k)
     assert nv.nvfp4_get_device_status() == 0
 
 
