@@ -9,19 +9,26 @@
 // quantizer writes scales row-major; nvfp4_swizzle_block_scales re-lays them (zero padding).
 //
 // nvfp4_gemm_nt is one hand-written tcgen05 kernel.  A persistent grid (one CTA per SM) walks the
-// 128 x 128 output tiles; per CTA:
-//   warp 0      (one thread) TMA: per stage a 128-row x 128-byte slab of each operand's codes
-//               (256 FP4 values along K, 128-byte swizzle) by cp.async.bulk.tensor, and the
-//               stage's 512-byte scale tiles of both operands by cp.async.bulk, into a ring of
-//               shared-memory stages completing on mbarriers;
-//   warp 1      owns the tensor memory (TMEM); one thread copies each stage's scale tiles into
-//               TMEM (tcgen05.cp 32x128b.warpx4) and issues the block-scaled FP4 products
+// 128 x 256 output tiles (128 rows of x, 256 rows of w); per CTA:
+//   warp 0      (one thread) TMA: per stage the 128-byte (256 FP4 values) K slab of the tile's
+//               128 rows of x and 256 rows of w (128-byte swizzle, cp.async.bulk.tensor) and the
+//               stage's 512-byte scale tiles (cp.async.bulk), into a 4-stage shared-memory ring
+//               completing on mbarriers;
+//   warps 10-13 write each stage's scale tiles into a TMEM slot with tcgen05.st (every lane
+//               quarter holds a whole tile, the layout the block-scaled product reads);
+//   warp 1      owns the tensor memory (TMEM); one thread issues the block-scaled FP4 products
 //               (tcgen05.mma kind::mxf4nvf4, scale_vec::4X: E2M1 x E2M1 with one UE4M3 scale per
-//               16 values along K, FP32 accumulation in TMEM, K = 64 per instruction), then
-//               releases the stage (tcgen05.commit) and, per tile, hands the accumulator over;
-//   warps 2-5   epilogue: each reads its 32 TMEM lanes (= 32 rows of the tile) with tcgen05.ld
-//               and writes y[m][n] = bf16(fp32(fp32(D[m][n] * S_x[m]) * S_w)) straight to global
-//               memory, while the MMA fills the other of the two accumulator buffers.
+//               16 values along K, M = 128, N = 256, K = 64, FP32 accumulation in TMEM), releases
+//               each stage with tcgen05.commit and hands the finished accumulator over;
+//   warps 2-9   epilogue: warp w reads TMEM lanes 32*(w % 4) .. +31 (its 32 rows) and 128 of the
+//               256 accumulator columns with tcgen05.ld and writes
+//               y[m][n] = bf16(fp32(fp32(D[m][n] * S_x[m]) * S_w)) straight to global memory.
+// Measured on GB300 (16384 x 2048 x 7168): consecutive products into one accumulator run about
+// 250 cycles apart whatever N is, so each product takes the widest N (256) the accumulator and
+// the scale slots leave room for in TMEM (512 columns); products into independent accumulators
+// overlap, but two 256-column accumulators leave no columns for the scales.  Scale copies issued
+// by the product thread (tcgen05.cp) wait in the same in-order pipe as the products (measured
+// 286 -> 164 us without them), hence the separate scale warps.
 // Every mbarrier wait is bounded; a wait that runs out records NVFP4_ERR_TIMEOUT, tells the other
 // roles to stop, and the CTA waits for its own copies and products in flight and frees its TMEM
 // before it returns.
@@ -253,13 +260,17 @@ struct GemmParams {
 
 // Waits for the barrier phase of the given parity; gives up when another role has stopped the
 // CTA (abort flag) or after timeout_ns (then it records the timeout and stops the others).
+// Roles whose events are far apart poll with a pause of sleep_ns between rounds, which leaves
+// the issue slots and shared-memory port to the roles on the critical path (measured: 4% faster).
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
-                                           volatile int* abort_flag, int* status) {
+                                           volatile int* abort_flag, int* status,
+                                           int sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_ns();
   while (true) {
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 4; ++i)
       if (mbar_try_wait(bar, parity)) return true;
+    if (sleep_ns > 0) __nanosleep(sleep_ns);
     if (*abort_flag) return false;
     if (global_ns() - start > timeout_ns) {
       *abort_flag = 1;
@@ -272,9 +283,10 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint6
 // The same, for a whole warp: lane 0 waits and the warp follows its answer, so warp-wide
 // tcgen05 instructions after it run on all 32 lanes or on none.
 __device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
-                                                volatile int* abort_flag, int* status, int lane) {
+                                                volatile int* abort_flag, int* status, int lane,
+                                                int sleep_ns = 0) {
   int ok = 0;
-  if (lane == 0) ok = wait_phase(bar, parity, timeout_ns, abort_flag, status) ? 1 : 0;
+  if (lane == 0) ok = wait_phase(bar, parity, timeout_ns, abort_flag, status, sleep_ns) ? 1 : 0;
   return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
@@ -340,7 +352,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int hv = live_halves(p, nt);
         for (int ks = 0; ks < p.kstages; ++ks, ++g) {
           const int s = g % kStages;
-          if (!wait_phase(&empty[s], ((g / kStages) & 1) ^ 1, tmo, abort_flag, p.status)) {
+          if (!wait_phase(&empty[s], ((g / kStages) & 1) ^ 1, tmo, abort_flag, p.status, 64)) {
             ok = false;
             break;
           }
@@ -409,7 +421,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const float sw = p.sw[0];
     int it = 0;
     for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
-      if (!warp_wait_phase(acc_full, it & 1, tmo, abort_flag, p.status, lane)) break;
+      if (!warp_wait_phase(acc_full, it & 1, tmo, abort_flag, p.status, lane, 1000)) break;
       tc_fence_after();
       const int mt = tile / p.tiles_n, nt = tile - (tile / p.tiles_n) * p.tiles_n;
       const int row = mt * kTileM + r_in_tile;
@@ -459,7 +471,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int hv = live_halves(p, tile - (tile / p.tiles_n) * p.tiles_n);
       for (int ks = 0; ks < p.kstages; ++ks, ++g) {
         const int s = g % kStages;
-        if (!warp_wait_phase(&full[s], (g / kStages) & 1, tmo, abort_flag, p.status, lane)) {
+        if (!warp_wait_phase(&full[s], (g / kStages) & 1, tmo, abort_flag, p.status, lane, 128)) {
           ok = false;
           break;
         }
