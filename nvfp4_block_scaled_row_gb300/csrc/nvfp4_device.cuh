@@ -359,38 +359,11 @@ __device__ __forceinline__ uint32_t f16x2_from_f32x2(f32x2 v) {
   return d;
 }
 
-// Per half: a - b in FP16 (RNE).
-__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// Per half: d*d + acc as one FP16 fused multiply-add (RNE).
-__device__ __forceinline__ uint32_t fma_f16x2(uint32_t d, uint32_t acc) {
+// Per half: a*b + c as one FP16 fused multiply-add (RNE).
+__device__ __forceinline__ uint32_t fma_f16x2(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t r;
-  asm("fma.rn.f16x2 %0, %1, %1, %2;" : "=r"(r) : "r"(d), "r"(acc));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
   return r;
-}
-
-// f16(f16(a.lo + a.hi) + f16(b.lo + b.hi)) as FP32 (exact widening).
-__device__ __forceinline__ float f16_sum_of_halves(uint32_t a, uint32_t b) {
-  float r;
-  asm("{\n\t.reg .f16 al, ah, bl, bh, sa, sb, s;\n\t"
-      "mov.b32 {al, ah}, %1;\n\t"
-      "mov.b32 {bl, bh}, %2;\n\t"
-      "add.rn.f16 sa, al, ah;\n\t"
-      "add.rn.f16 sb, bl, bh;\n\t"
-      "add.rn.f16 s, sa, sb;\n\t"
-      "cvt.f32.f16 %0, s;\n\t}"
-      : "=f"(r)
-      : "r"(a), "r"(b));
-  return r;
-}
-
-// The low FP16 half of a word, widened exactly to FP32.
-__device__ __forceinline__ float f16_low_to_f32(uint32_t w) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
 }
 
 // FP32 pair to BF16 pair (RNE): .x to the low half.

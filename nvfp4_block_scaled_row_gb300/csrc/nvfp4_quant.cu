@@ -112,39 +112,31 @@ __device__ __forceinline__ f32x2 block_errors(const f32x2 (&z)[8], const Codes& 
   return acc;
 }
 
-// One candidate with the FP16 selector's error (see encode_candidate_fp16).
-struct Candidate {
-  uint32_t cw[2];
-  uint32_t r[8];
-  float err;
-};
-
-// The FP16 reading of the 4/6 fast path ("NVFP4 RL" blog, Sec. 4, "The optimization": cast to
-// FP16 losslessly and scale the target down by its inverse): the same targets and codes as
-// encode_candidate, but the block error is taken in FP16 in the scaled-down domain,
-//   delta = f16(f16(t) - r),  E[h][p] = FP16 FMA chains,  E = f16(f16(EA0 + EA1) + f16(EB0 + EB1)),
-// and brought back to a common scale in FP32 as fp32(E) * s^2 (s^2 exact).
-__device__ __forceinline__ Candidate encode_candidate_fp16(const f32x2 (&z)[8], const ScaleEntry e) {
-  Candidate c;
-  const f32x2 inv2 = pack2(e.inv, e.inv);
-  f32x2 t[8];
+// The FP16 reading of the 4/6 fast path ("NVFP4 RL" blog, Sec. 4, "The optimization": cast
+// losslessly to FP16 and scale the target down by its inverse instead of scaling the candidate
+// up): per candidate, the residual of the FP16 target z_h = f16(z) against the exact FP16
+// candidate q*s, d = f16(z_h - q*s) (one FP16 FMA of the decoded pair with -s), and its square
+// summed in FP32 (exact: d has 11 significant bits) from +0 in ascending element order.  Returns
+// (scale-to-6 error, scale-to-4 error).
+__device__ __forceinline__ f32x2 block_errors_fp16(const f32x2 (&z)[8], const Codes& c6,
+                                                   uint32_t ns6, const Codes& c4, uint32_t ns4) {
+  float e6 = 0.0f, e4 = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) t[j] = mul2(z[j], inv2);
-  uint32_t rA[4], rB[4];
-  c.cw[0] = e2m1x8_encode_decode(t[0], t[1], t[2], t[3], rA);
-  c.cw[1] = e2m1x8_encode_decode(t[4], t[5], t[6], t[7], rB);
-  uint32_t accA = 0u, accB = 0u;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    accA = fma_f16x2(sub_f16x2(f16x2_from_f32x2(t[j]), rA[j]), accA);
-    accB = fma_f16x2(sub_f16x2(f16x2_from_f32x2(t[4 + j]), rB[j]), accB);
-    c.r[j] = rA[j];
-    c.r[4 + j] = rB[j];
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t zh = f16x2_from_f32x2(z[j]);
+    const uint32_t d6 = fma_f16x2(c6.r[j], ns6, zh);
+    const uint32_t d4 = fma_f16x2(c4.r[j], ns4, zh);
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %2;\n\t"
+        "mov.b32 {b0, b1}, %3;\n\t"
+        "fma.rn.f32.f16 %0, a0, a0, %0;\n\t"
+        "fma.rn.f32.f16 %1, b0, b0, %1;\n\t"
+        "fma.rn.f32.f16 %0, a1, a1, %0;\n\t"
+        "fma.rn.f32.f16 %1, b1, b1, %1;\n\t}"
+        : "+f"(e6), "+f"(e4)
+        : "r"(d6), "r"(d4));
   }
-  const float E = f16_sum_of_halves(accA, accB);
-  const float s = -f16_low_to_f32(e.neg_s_h2);
-  c.err = __fmul_rn(E, __fmul_rn(s, s));
-  return c;
+  return pack2(e6, e4);
 }
 
 // Encodes one 16-element block with block amax m: both candidates (scale-to-6 only in mode six),
@@ -177,31 +169,20 @@ __device__ __forceinline__ void encode_block(const uint4 lo, const uint4 hi, flo
   const ScaleEntry e6 = tab[b6];
   bool pick4 = false;
   ScaleEntry e4{};
-  uint32_t w0, w1;          // the chosen code words
-  const uint32_t* r;        // the chosen decoded pairs
-  Codes c6, c4;
-  Candidate h6, h4;
-  if (kMode == kModeFourOverSixFp16) {
+  Codes c4{};
+  const Codes c6 = encode_codes(z, e6.inv);
+  if (kMode != kModeSix) {
     e4 = tab[b4];
-    h6 = encode_candidate_fp16(z, e6);
-    h4 = encode_candidate_fp16(z, e4);
-    pick4 = h4.err < h6.err;  // ties go to 6
-    w0 = pick4 ? h4.cw[0] : h6.cw[0];
-    w1 = pick4 ? h4.cw[1] : h6.cw[1];
-    r = pick4 ? h4.r : h6.r;
-  } else {
-    c6 = encode_codes(z, e6.inv);
-    if (kMode == kModeFourOverSix) {
-      e4 = tab[b4];
-      c4 = encode_codes(z, e4.inv);
-      float err6, err4;
-      unpack2(block_errors(z, c6, e6.neg_s_h2, c4, e4.neg_s_h2), err6, err4);
-      pick4 = err4 < err6;  // ties go to 6
-    }
-    w0 = pick4 ? c4.cw[0] : c6.cw[0];
-    w1 = pick4 ? c4.cw[1] : c6.cw[1];
-    r = pick4 ? c4.r : c6.r;
+    c4 = encode_codes(z, e4.inv);
+    float err6, err4;
+    unpack2(kMode == kModeFourOverSixFp16 ? block_errors_fp16(z, c6, e6.neg_s_h2, c4, e4.neg_s_h2)
+                                          : block_errors(z, c6, e6.neg_s_h2, c4, e4.neg_s_h2),
+            err6, err4);
+    pick4 = err4 < err6;  // ties go to 6
   }
+  const uint32_t w0 = pick4 ? c4.cw[0] : c6.cw[0];  // the chosen code words
+  const uint32_t w1 = pick4 ? c4.cw[1] : c6.cw[1];
+  const uint32_t* r = pick4 ? c4.r : c6.r;          // the chosen decoded pairs
   *reinterpret_cast<uint2*>(codes_blk) = make_uint2(w0, w1);
   *scale_ptr = static_cast<uint8_t>(pick4 ? b4 : b6);
 

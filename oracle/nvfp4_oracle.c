@@ -204,34 +204,24 @@ static int quantize_candidate(const float x[ORACLE_BLOCK], float m, float S_enc,
   return sbyte;
 }
 
-/* The FP16 reading of the 4/6 fast path ([RL-blog] Sec. 4, "The optimization": cast losslessly
- * to FP16 and scale the target down by its inverse instead of scaling the candidate up): the same
- * scaled targets t and codes as the FP32 candidate, the target cast to FP16, the residual
- * delta = f16(f16(t) - r) (r exact in FP16), two FP16 FMA chains per half (elements 8h+p+2k,
- * k ascending), E = f16(f16(E[0][0] + E[0][1]) + f16(E[1][0] + E[1][1])), and the error brought
- * back to the common scale in FP32: e = fp32(E) * (s*s) (s*s exact). */
+/* The FP16 reading of the 4/6 fast path ([RL-blog] Sec. 4, "The optimization": do the casting
+ * losslessly in FP16 and, rather than multiplying the candidate up by the fractional scales,
+ * scale the target down by their inverse).  The candidate value q*s is exact in FP16 (an E2M1
+ * value times an E4M3 value has at most 6 significant bits and magnitude at most 2688); the
+ * target is x scaled down by the inverse of the per-token scale, z = fp32(x * S_enc), cast to
+ * FP16; the residual is one FP16 rounding of the exact z_h - q*s; its square is exact in FP32 and
+ * the squares are summed in FP32 from +0 in ascending element order, e = fma(d_i, d_i, e). */
 static float candidate_error_fp16(const float x[ORACLE_BLOCK], float S_enc, float s,
                                   const uint8_t code[ORACLE_BLOCK]) {
-  float inv = (s == 0.0f) ? 0.0f : 1.0f / s;
-  double d[ORACLE_BLOCK];
+  float e = 0.0f;
   for (int i = 0; i < ORACLE_BLOCK; ++i) {
     float z = x[i] * S_enc;
-    float t = z * inv;
-    double th = oracle_f16_round((double)t);
-    d[i] = oracle_f16_round(th - oracle_e2m1_value(code[i]));
+    double zh = oracle_f16_round((double)z);
+    double qs = oracle_e2m1_value(code[i]) * (double)s; /* exact */
+    float d = (float)oracle_f16_round(zh - qs);
+    e = fmaf(d, d, e);
   }
-  double E[2][2];
-  for (int h = 0; h < 2; ++h)
-    for (int p = 0; p < 2; ++p) {
-      double acc = 0.0;
-      for (int k = 0; k < 4; ++k) {
-        double di = d[8 * h + p + 2 * k];
-        acc = oracle_f16_round(di * di + acc); /* one FP16 fma: exact in double, one rounding */
-      }
-      E[h][p] = acc;
-    }
-  double Eh = oracle_f16_round(oracle_f16_round(E[0][0] + E[0][1]) + oracle_f16_round(E[1][0] + E[1][1]));
-  return (float)Eh * (s * s);
+  return e;
 }
 
 /* One block: both candidates (only scale-to-6 in mode six), then the 4/6 choice ([RL-blog] Sec. 4).

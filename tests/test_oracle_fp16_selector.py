@@ -1,7 +1,12 @@
-"""Pins for the FP16 reading of the 4/6 fast path (mode four_over_six_fp16): its FP16 rounding is
-IEEE binary16 (checked against torch's float16), its candidates are the FP32 path's, so outputs
-differ from mode four_over_six only in blocks whose choice flips, and the choice agrees with the
-FP32 choice on far more than 99.9% of blocks (the pages quote > 99.97% for their fast path)."""
+"""Pins for the FP16 reading of the 4/6 fast path (mode four_over_six_fp16): the target
+z = x * S_enc cast to FP16, the exact FP16 candidate q * s, one FP16 rounding of the residual, and
+the squares summed in FP32 in ascending element order.  Its FP16 rounding is IEEE binary16
+(checked against torch's float16); its candidates are the FP32 path's, so outputs differ from mode
+four_over_six only in blocks whose choice flips; the sum runs in FP32 in element order (the
+chain-order blocks give the FP32 path's values); and the choice agrees with the FP32 choice on
+99.85-99.95% of blocks -- never all of them, since the FP16 target moves near ties.  (The pages
+quote > 99.97% on their tensors; on these workloads 1-2% of blocks have a relative gap between the
+two candidates' errors below 1%, within reach of FP16 rounding noise.)"""
 import numpy as np
 import pytest
 import torch
@@ -42,10 +47,9 @@ def test_outputs_differ_only_where_the_choice_flips(inputs):
 
 
 def test_choice_agreement_with_fp32(inputs):
-    """Counts choices that differ from the FP32 choice.  Exact FP32 ties (e4 == e6, which the FP32
-    rule sends to 6) are where FP16 rounding noise most often decides differently; every other
-    disagreement is a near tie.  The FP16 choice never costs more than 1% block error: each FP16
-    rounding is within 2^-11 relative and a block error goes through about 20 of them."""
+    """Counts choices that differ from the FP32 choice (exact FP32 ties, e4 == e6, reported apart).
+    Each FP16 rounding of a target is within 2^-11 of it, so only near ties can flip, and the FP16
+    choice never costs more than 1% block error (FP32 errors of the two candidates compared)."""
     agree = total = ties = agree_non_tie = 0
     for xb in inputs:
         a = oracle.quantize(xb, F4, diagnostics=True)
@@ -65,4 +69,18 @@ def test_choice_agreement_with_fp32(inputs):
     rate_non_tie = agree_non_tie / (total - ties)
     print(f"FP16 selector: agrees with the FP32 choice on {rate:.4%} of {total} blocks, "
           f"{rate_non_tie:.4%} of the {total - ties} blocks without an exact FP32 tie")
-    assert rate > 0.995 and rate_non_tie > 0.998
+    assert 0.9985 < rate < 0.9996 and rate_non_tie > 0.9985
+
+
+def test_fp16_errors_sum_in_fp32_in_element_order():
+    """On the chain-order blocks (every target exact in FP16) the FP16 reading reproduces the FP32
+    path's chain values and choices: the sum is FP32, ascending (an FP16 sum would round 4096 +
+    13 * 2^-14 to 4096 and tie both blocks)."""
+    from test_oracle_method import chain_order_row
+
+    xb = chain_order_row()
+    out = oracle.quantize(xb, F16, diagnostics=True)
+    assert list(out["choice"][0]) == [0, 1]
+    lo, hi = np.float32(4096.0), np.float32(4096.0 + 2.0 ** -10)
+    assert out["errs"][0, 0].tolist() == [lo, hi]
+    assert out["errs"][0, 1].tolist() == [hi, lo]

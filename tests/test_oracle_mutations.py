@@ -56,7 +56,11 @@ MUTATIONS = [
      "double v = (fabs(hi - tc) < fabs(lo - tc)) ? hi : lo;"),
     ("guided takes the farther neighbour", "double v = (fabs(hi - rv) < fabs(lo - rv)) ? hi : lo;",
      "double v = (fabs(hi - rv) < fabs(lo - rv)) ? lo : hi;"),
-    ("fp16 error scaled by s", "return (float)Eh * (s * s);", "return (float)Eh * s;"),
+    ("fp16 candidate without its scale", "double qs = oracle_e2m1_value(code[i]) * (double)s; /* exact */",
+     "double qs = oracle_e2m1_value(code[i]); /* exact */"),
+    ("fp16 target not rounded", "double zh = oracle_f16_round((double)z);", "double zh = (double)z;"),
+    ("fp16 sum in fp16", "    e = fmaf(d, d, e);\n  }\n  return e;",
+     "    e = (float)oracle_f16_round((double)d * d + e);\n  }\n  return e;"),
 ]
 
 
@@ -94,6 +98,7 @@ def _pins(inputs):
     T.test_choice_is_a_neighbour_and_never_further_than_rtn(1)
     H.test_outputs_differ_only_where_the_choice_flips(inputs)
     H.test_choice_agreement_with_fp32(inputs)
+    H.test_fp16_errors_sum_in_fp32_in_element_order()
 
 
 @pytest.fixture(scope="module")
