@@ -94,7 +94,8 @@ typedef enum {
  *                 and a violation records NVFP4_ERR_OFFSETS.  NULL (with num_groups == 0) skips it.
  *   mode          NVFP4_MODE_SIX or NVFP4_MODE_FOUR_OVER_SIX.
  *   codes, block_scales, row_scale   outputs as laid out above.
- * Supported cols: 16 <= cols <= 32768, cols % 16 == 0. */
+ * Supported cols: 16 <= cols <= 65536, cols % 16 == 0 (rows wider than 32768 are staged by all
+ * 16 warps of a CTA in one shared-memory slot each, without copy/compute overlap: slower). */
 nvfp4_status nvfp4_quantize_rowwise(const void* x, int64_t rows, int64_t cols,
                                     const int32_t* group_offsets, int32_t num_groups,
                                     nvfp4_mode mode, uint8_t* codes, uint8_t* block_scales,

@@ -14,10 +14,10 @@
 namespace nvfp4 {
 
 constexpr int kBlockElems = 16;          // elements per E4M3-scaled block
-constexpr int kMaxCols = 32768;          // widest row the shared-memory ring supports
+constexpr int kMaxCols = 65536;          // widest row the shared-memory ring supports
 constexpr int kMaxWarpsPerCta = 16;
 constexpr int kMaxStages = 4;
-constexpr int kMaxTeam = 8;              // warps that share one row
+constexpr int kMaxTeam = 16;             // warps that share one row (16: the whole CTA)
 constexpr int kMaxBlocksPerLane = 8;     // 16-element blocks one lane owns per row (<= 8 KB slots)
 constexpr int kAmaxMaxPartials = 1024;   // per-tensor amax: partial maxima in the workspace
 

@@ -186,7 +186,7 @@ def _edge_matrix(rows, cols, seed):
     return t.to(DEV)
 
 
-@pytest.mark.parametrize("cols", [16, 32, 48, 496, 512, 2064, 7168, 7184, 16384, 32768])
+@pytest.mark.parametrize("cols", [16, 32, 48, 496, 512, 2064, 7168, 7184, 16384, 32768, 65536])
 def test_edge_values_and_ragged_widths(cols):
     rows = 3 if cols >= 16384 else 37
     x = _edge_matrix(rows, cols, seed=cols)
@@ -295,12 +295,13 @@ def test_bounded_wait_reports_timeout():
 
 
 @pytest.mark.parametrize("cols,op", [(7168, "rowwise"), (7168, "fused"), (7168, "tensor"),
-                                     (7168, "residual"), (2048, "rowwise"), (32768, "rowwise")])
+                                     (7168, "residual"), (2048, "rowwise"), (32768, "rowwise"),
+                                     (65536, "rowwise")])
 def test_quantize_ring_timeout_path(cols, op):
     """The quantize kernel's own failure branches: with one row's copies withheld, the warps that
     own it give up after 1 ms, record NVFP4_ERR_TIMEOUT, drain their copies still in flight and
-    return (a team of several warps -- 2 for 7168-wide rows, 8 for 32768 -- leaves together behind
-    its barrier); the next ordinary call on the same context is bit-exact."""
+    return (a team of several warps -- 2 for 7168-wide rows, 8 for 32768, 16 for 65536 -- leaves
+    together behind its barrier); the next ordinary call on the same context is bit-exact."""
     if cols == 2048:
         x = synth.generate(0, device=DEV, rows=96)["x"]
     elif cols == 7168:
@@ -337,7 +338,7 @@ def test_host_validation_errors():
     with pytest.raises(ValueError):
         nv.nvfp4_quantize_rowwise(x.cpu())
     with pytest.raises(nv.Nvfp4Error) as e:
-        nv.nvfp4_quantize_rowwise(torch.empty((4, 65536), dtype=torch.bfloat16, device=DEV))
+        nv.nvfp4_quantize_rowwise(torch.empty((4, 65536 + 16), dtype=torch.bfloat16, device=DEV))
     assert e.value.status == 2
 
 
@@ -440,7 +441,7 @@ def test_residual_workloads(index, rows):
     check_residual(x, SIX)
 
 
-@pytest.mark.parametrize("cols", [16, 48, 2064, 7168, 7184, 32768])
+@pytest.mark.parametrize("cols", [16, 48, 2064, 7168, 7184, 32768, 65536])
 def test_residual_edge_values(cols):
     check_residual(_edge_matrix(3 if cols >= 16384 else 21, cols, seed=cols + 1))
 
