@@ -25,9 +25,14 @@ constexpr int kAmaxMaxPartials = 1024;   // per-tensor amax: partial maxima in t
 constexpr int kTableBytes = 256 * 8;                          // one ScaleEntry per E4M3 byte
 constexpr int kXchBytes = 4 * kMaxWarpsPerCta * 4;            // row-amax partials: 2 parities x 2 tensors
 constexpr int kAbortBytes = kMaxWarpsPerCta * 4;              // per-team abort flags
-constexpr int kBarrierBytes = kMaxWarpsPerCta * kMaxStages * 8;
-constexpr int kHeaderBytes =
-    ((kTableBytes + kXchBytes + kAbortBytes + kBarrierBytes + 127) / 128) * 128;
+constexpr int kWorkQueue = 8;                                 // work requests in flight or unread
+constexpr int kWorkQueueBytes = kWorkQueue * 16 + 2 * kWorkQueue * 8;  // answers, full/free barriers
+constexpr int kFixedHeaderBytes = kTableBytes + kXchBytes + kAbortBytes + kWorkQueueBytes;
+
+// Header bytes for `warps` warps with `stages` ring slots each (one copy barrier per slot).
+__host__ __device__ constexpr int ring_header_bytes(int warps, int stages) {
+  return ((kFixedHeaderBytes + warps * stages * 8 + 127) / 128) * 128;
+}
 
 // Device status codes (same numbers as nvfp4_status in include/nvfp4.h).
 constexpr int kStatusTimeout = 5;
@@ -151,6 +156,40 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
       if (mbar_try_wait(bar, parity)) return true;
     if (global_ns() - start > timeout_ns) return false;
   }
+}
+
+// One arrival (count 1) on a shared-memory barrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Cluster launch control: asks the hardware to cancel one CTA of this grid that has not started
+// yet; the 16-byte answer lands in `answer` and completes `bar` (16 transaction bytes, which the
+// caller announces with mbar_arrive_expect_tx first).  One thread issues it.
+__device__ __forceinline__ void launch_control_request(void* answer, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
+      " [%0], [%1];" ::"r"(smem_addr(answer)),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Decodes an answer: returns true and the cancelled CTA's x index when the request succeeded
+// (the index is only read from a successful answer).
+__device__ __forceinline__ bool launch_control_answer(const void* answer, uint32_t& ctaid_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 h;\n\t"
+      "ld.shared.b128 h, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "mov.u32 %1, 0;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(smem_addr(answer))
+      : "memory");
+  ctaid_x = x;
+  return ok != 0;
 }
 
 // Bulk prefetch of [gsrc, gsrc + bytes) into L2 (a hint: no data moves to this SM).

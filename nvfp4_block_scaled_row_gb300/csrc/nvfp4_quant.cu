@@ -248,14 +248,28 @@ __device__ __forceinline__ uint32_t block_max_word(const uint4 A, const uint4 B)
                         max_abs_bf16x2(max_abs_bf16x2(B.x, B.y), max_abs_bf16x2(B.z, B.w)));
 }
 
-// Shared-memory layout: [table | amax exchange | abort flags | barriers] (kHeaderBytes), then the
-// ring: warp w owns `stages` slots of `slot_bytes`.
+// Shared-memory layout: [table | amax exchange | abort flags | work queue | copy barriers]
+// (ring_header_bytes), then the ring: warp w owns `stages` slots of `slot_bytes`.
 //
 // Work split: a team of `team` warps shares each row; warp t of a team owns the blocks
-// [t*bpw, min(nblk, (t+1)*bpw)) and stages only that part of the row.  Teams take rows
-// gt, gt + NT, gt + 2NT, ... (gt = global team index, NT = number of teams).  With more than one
-// warp per team the row amax is combined through shared memory behind a named barrier; if any
-// member's copy times out, all members leave together after that barrier.
+// [t*bpw, min(nblk, (t+1)*bpw)) and stages only that part of the row.  Two schedules:
+//  - dynamic (the fused round trip, bound by HBM): work unit u is the rows [u*T, u*T + T) of a
+//    CTA with T teams, one row per team.  The grid has one CTA per unit (or gridDim.x < units
+//    under a launch-shape override, when CTA c walks the units c, c + gridDim.x, ...); a CTA
+//    starts with unit blockIdx.x, and when its walk ends it takes over the walk of a CTA of the
+//    grid that has not started yet, by cluster launch control, until none is left.  The units go
+//    to SMs in order as they free up, so the rows in flight stay one compact window of the
+//    matrix and all SMs finish within about one unit of each other.  Thread 0 issues the
+//    requests strictly one after another, each only after the previous one was answered with a
+//    success (so none follows a failed one, and none can succeed after one failed); every warp
+//    reads every answer in order and stops at the first failure.
+//  - static (the issue-bound quantize-only and residual kernels, for which a request per unit
+//    costs more than it balances): a persistent grid, team gt = team * gridDim.x + blockIdx.x
+//    takes the rows gt, gt + NT, gt + 2NT, ... (NT = number of teams); consecutive teams sit on
+//    different SMs, so uneven row counts put at most one extra row on an SM.
+// With more than one warp per team the row amax is combined
+// through shared memory behind a named barrier; if any member's copy times out, all members
+// leave together after that barrier.
 // kNB > 0: every lane owns exactly kNB blocks of each row (the row's blocks split evenly over the
 // team, 32 * kNB per warp), so the block loops have a fixed trip count (residual kernels: only
 // the third pass's loop); kNB = 0: any split.
@@ -265,8 +279,10 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
   ScaleEntry* tab = reinterpret_cast<ScaleEntry*>(smem);
   float* xch = reinterpret_cast<float*>(smem + kTableBytes);
   int* abort_flag = reinterpret_cast<int*>(smem + kTableBytes + kXchBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTableBytes + kXchBytes + kAbortBytes);
-  unsigned char* ring = smem + kHeaderBytes;
+  unsigned char* answers = smem + kTableBytes + kXchBytes + kAbortBytes;  // kWorkQueue x 16 B
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(answers + kWorkQueue * 16);
+  uint64_t* q_free = q_full + kWorkQueue;
+  uint64_t* bars = q_free + kWorkQueue;
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -276,6 +292,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
   const int teams = nwarps / TW;
   const int team = warp / TW;
   const int tw = warp - team * TW;
+  unsigned char* ring = smem + ring_header_bytes(nwarps, S);
   uint64_t* my_bars = bars + warp * S;
   unsigned char* my_ring = ring + static_cast<size_t>(warp) * S * p.slot_bytes;
 
@@ -283,81 +300,166 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
   if (threadIdx.x < kMaxWarpsPerCta) abort_flag[threadIdx.x] = 0;
   if (lane == 0)
     for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kWorkQueue; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_free[i], nwarps);
+    }
   fence_barrier_init();
   __syncthreads();
+
+  // ---- work units ----
+  constexpr bool kDynamic = kFused;
+  const int64_t units = (p.rows + teams - 1) / teams;
+  const int64_t G = gridDim.x;
+  const int64_t gt = static_cast<int64_t>(team) * G + blockIdx.x;  // static schedule
+  const int64_t NT = G * teams;
+  // The row of this team in unit u (dynamic) or step u (static); p.rows for none.
+  auto row_of = [&](int64_t u) -> int64_t {
+    if (u < 0) return p.rows;
+    if constexpr (kDynamic) return u * teams + team;
+    return gt + u * NT;
+  };
+  // When warp 0 reads answer j, thread 0 first makes sure requests up to j + kLead - 1 are out,
+  // so the other warps rarely wait for one.
+  constexpr int kLead = 3;
+  // Thread 0: requests issued so far (request j >= 1 uses queue entry j % kWorkQueue for the
+  // ((j - 1) / kWorkQueue)-th time), and whether it has stopped issuing.
+  int requested = 0;
+  bool stop_requests = false;
+  auto request_next = [&]() {
+    const int j = requested + 1;
+    if (j >= 2) {  // the previous request must have been answered with a success
+      const int q = (j - 1) % kWorkQueue;
+      uint32_t unused;
+      if (!mbar_wait_bounded(&q_full[q], static_cast<uint32_t>(((j - 2) / kWorkQueue) & 1),
+                             p.timeout_ns)) {
+        record_status(p.status, kStatusTimeout);
+        stop_requests = true;
+        return;
+      }
+      if (!launch_control_answer(answers + q * 16, unused)) {
+        stop_requests = true;
+        return;
+      }
+    }
+    const int q = j % kWorkQueue;
+    const int use = (j - 1) / kWorkQueue;
+    // The entry's previous answer must have been read by every warp.
+    if (use >= 1 && !mbar_wait_bounded(&q_free[q], static_cast<uint32_t>((use - 1) & 1),
+                                       p.timeout_ns)) {
+      record_status(p.status, kStatusTimeout);
+      stop_requests = true;
+      return;
+    }
+    mbar_arrive_expect_tx(&q_full[q], 16);
+    launch_control_request(answers + q * 16, &q_full[q]);
+    requested = j;
+  };
+  // Before thread 0 leaves early: wait (bounded) for its last request's answer, so that it does
+  // not land after the CTA is gone.
+  auto drain_requests = [&]() {
+    if (requested >= 1)
+      (void)mbar_wait_bounded(&q_full[requested % kWorkQueue],
+                              static_cast<uint32_t>(((requested - 1) / kWorkQueue) & 1),
+                              p.drain_timeout_ns);
+  };
+  // Warp-collective: the next answer in order (-1 once one failed; every warp reads each once).
+  int answers_read = 0;
+  bool ended = false;
+  auto read_answer = [&]() -> int64_t {
+    if (ended) return -1;
+    int64_t u = -1;
+    if (lane == 0) {
+      const int j = answers_read + 1;
+      if (threadIdx.x == 0)
+        while (!stop_requests && requested < j + kLead - 1) request_next();
+      const int q = j % kWorkQueue;
+      if (mbar_wait_bounded(&q_full[q], static_cast<uint32_t>(((j - 1) / kWorkQueue) & 1),
+                            p.timeout_ns)) {
+        uint32_t x;
+        if (launch_control_answer(answers + q * 16, x)) u = static_cast<int64_t>(x);
+        mbar_arrive(&q_free[q]);
+      } else {
+        record_status(p.status, kStatusTimeout);
+      }
+      answers_read = j;
+    }
+    u = __shfl_sync(0xFFFFFFFFu, u, 0);
+    if (u < 0 || u >= units) {
+      ended = true;
+      u = -1;
+    }
+    return u;
+  };
+  // The unit after `u` in this CTA's order (-1: none left).
+  auto next_unit = [&](int64_t u) -> int64_t {
+    if (u < 0) return -1;
+    if constexpr (kDynamic) return u + G < units ? u + G : read_answer();
+    return gt + (u + 1) * NT < p.rows ? u + 1 : -1;
+  };
+  // Lane s (s < S) holds the unit of the steps that use ring slot s; `last` is the unit of the
+  // latest step assigned so far.
+  int64_t slot_unit = -1;
+  int64_t last = kDynamic ? static_cast<int64_t>(blockIdx.x) : (gt < p.rows ? 0 : -1);
+  if (lane == 0) slot_unit = last;
+  for (int s = 1; s < S; ++s) {
+    last = next_unit(last);
+    if (lane == s) slot_unit = last;
+  }
+
   // Everything above touched only this CTA's shared memory, so it overlaps the previous kernel's
   // tail; global memory waits for that kernel (except the first row copies of a tensor-scale grid
   // that follows our amax kernel, see below).
-  if (!p.prologue_before_wait) {
-    // While the previous kernel finishes, pull this warp's first rows into L2 (coherent, so safe
-    // even if that kernel writes them); the copies after the wait then hit L2.  Measured: the
-    // fused round trip gains 2.3% prefetching all its ring's rows; quantize-only kernels lose 2%
-    // doing the same but gain 0.5-2.5% prefetching only the first row.  Residual kernels skip it.
-    const int pb0 = (warp % TW) * p.blocks_per_warp;
-    const int pb1 = min(p.cols / kBlockElems, pb0 + p.blocks_per_warp);
-    const int64_t pgt = kFused ? static_cast<int64_t>(blockIdx.x) * (nwarps / TW) + warp / TW
-                               : static_cast<int64_t>(warp / TW) * gridDim.x + blockIdx.x;
-    const int64_t pNT = static_cast<int64_t>(gridDim.x) * (nwarps / TW);
-    if (kFused && lane == 0 && pb1 > pb0)
-      for (int s = 0; s < S && pgt + s * pNT < p.rows; ++s)
-        bulk_prefetch_l2(p.x + (pgt + s * pNT) * p.cols + pb0 * 16,
-                         static_cast<uint32_t>(pb1 - pb0) * 32u);
-    if (!kFused && !kResidual && lane == 0 && pb1 > pb0 && pgt < p.rows)
-      bulk_prefetch_l2(p.x + pgt * p.cols + pb0 * 16, static_cast<uint32_t>(pb1 - pb0) * 32u);
-    pdl_wait();
-  }
-  pdl_trigger();
-
-  // Group offsets only need validating: every row is quantized independently of its group.
-  if (p.offsets != nullptr && blockIdx.x == 0 && warp == 0) {
-    bool bad = false;
-    for (int i = lane; i <= p.num_groups; i += 32) {
-      const int32_t v = p.offsets[i];
-      if (i == 0 && v != 0) bad = true;
-      if (i == p.num_groups && static_cast<int64_t>(v) != p.rows) bad = true;
-      if (i > 0 && p.offsets[i - 1] > v) bad = true;
-    }
-    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) record_status(p.status, kStatusOffsets);
-  }
-
   const int cols = p.cols;
   const int nblk = cols / kBlockElems;
   const int b0 = tw * p.blocks_per_warp;
   const int b1 = min(nblk, b0 + p.blocks_per_warp);
   const bool has_work = b1 > b0;
   const uint32_t chunk_bytes = has_work ? static_cast<uint32_t>(b1 - b0) * 32u : 0u;
-  // Quantize-only and residual kernels (issue-bound): gt = team * gridDim.x + blockIdx.x, so
-  // consecutive teams sit on different SMs and, when the rows do not divide evenly over the
-  // teams, the extra rows land one per SM instead of all on the first CTAs (an SM's time follows
-  // its row count).  The fused round trip (bound by HBM) keeps each CTA's teams on consecutive
-  // rows, gt = blockIdx.x * teams + team, measured 2% faster for it.
-  const int64_t gt = kFused ? static_cast<int64_t>(blockIdx.x) * teams + team
-                            : static_cast<int64_t>(team) * gridDim.x + blockIdx.x;
-  const int64_t NT = static_cast<int64_t>(gridDim.x) * teams;
+  if (!p.prologue_before_wait) {
+    // While the previous kernel finishes, pull this warp's first rows into L2 (coherent, so safe
+    // even if that kernel writes them); the copies after the wait then hit L2.  Measured: the
+    // fused round trip gains 2.3% prefetching all its ring's rows; quantize-only kernels lose 2%
+    // doing the same but gain 0.5-2.5% prefetching only the first row.  Residual kernels skip it.
+    const int np = kFused ? S : ((kResidual || !has_work) ? 0 : 1);
+    for (int s = 0; s < np; ++s) {
+      const int64_t r = row_of(__shfl_sync(0xFFFFFFFFu, slot_unit, s));
+      if (lane == 0 && has_work && r < p.rows)
+        bulk_prefetch_l2(p.x + r * cols + b0 * 16, chunk_bytes);
+    }
+    pdl_wait();
+  }
+  pdl_trigger();
+
   const uint64_t policy = l2_evict_first_policy();
   const int h0 = (lane >> 2) & 1;  // which 16-byte half of its block this lane reads first
 
-  // Prologue: fill the ring with this warp's part of the team's first rows.  (The self-test's
-  // withheld row is never copied, so its slot's barrier never completes.)
-  int64_t issued = 0;
+  // Copies in flight (lane 0): bit s of `pending` is set while slot s has one; bit s of `phase`
+  // is the parity of the slot barrier's next phase.  (The self-test's withheld row is never
+  // copied, so its step's wait runs out.)
+  uint32_t pending = 0, phase = 0;
   auto issue = [&](int slot_index, int64_t row) {
     if (row != p.withhold_row) {
       mbar_arrive_expect_tx(&my_bars[slot_index], chunk_bytes);
       bulk_load(my_ring + static_cast<size_t>(slot_index) * p.slot_bytes,
                 p.x + row * cols + b0 * 16, chunk_bytes, &my_bars[slot_index], policy);
+      pending |= 1u << slot_index;
     }
-    ++issued;
   };
-  // Before an early exit: wait (bounded) for this warp's copies still in flight, those of the
-  // ring steps k, k+1, ..., so that none lands after the warp is gone.
-  auto drain = [&](int64_t k) {
-    for (int64_t i = k; i < issued; ++i)
-      if (gt + i * NT != p.withhold_row)
-        (void)mbar_wait_bounded(&my_bars[i % S], static_cast<uint32_t>((i / S) & 1),
-                                p.drain_timeout_ns);
+  // Before an early exit (lane 0): wait (bounded) for this warp's copies still in flight, so that
+  // none lands after the warp is gone; thread 0 also waits for its last request's answer.
+  auto drain = [&]() {
+    for (int s = 0; s < S; ++s)
+      if ((pending >> s) & 1u)
+        (void)mbar_wait_bounded(&my_bars[s], (phase >> s) & 1u, p.drain_timeout_ns);
+    if (threadIdx.x == 0) drain_requests();
   };
-  if (lane == 0 && has_work)
-    for (int s = 0; s < S && gt + s * NT < p.rows; ++s) issue(s, gt + s * NT);
+  // Prologue: fill the ring with this warp's part of the team's first rows.
+  for (int s = 0; s < S; ++s) {
+    const int64_t r = row_of(__shfl_sync(0xFFFFFFFFu, slot_unit, s));
+    if (lane == 0 && has_work && r < p.rows) issue(s, r);
+  }
 
   RowFactors f{};
   if (kTensor) {
@@ -369,23 +471,54 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
     f = row_factors<kMode>(a);
-    if (blockIdx.x == 0 && threadIdx.x == 0) p.scale_out[0] = f.S_dec;
   }
 
-  // Ring position of step k: slot k mod S, barrier phase parity (k / S) mod 2, both advanced
-  // incrementally (a 64-bit division per row costs more than the row's whole amax exchange).
-  int64_t k = 0;
+  // Once per grid, by the first warp of the team that has row 0 (dynamic: whichever CTA got unit
+  // 0; static: CTA 0): the tensor scale, and the group offsets, which only need validating (every
+  // row is quantized independently of its group).
+  auto grid_once = [&]() {
+    if (kTensor && lane == 0) p.scale_out[0] = f.S_dec;
+    if (p.offsets != nullptr) {
+      bool bad = false;
+      for (int i = lane; i <= p.num_groups; i += 32) {
+        const int32_t v = p.offsets[i];
+        if (i == 0 && v != 0) bad = true;
+        if (i == p.num_groups && static_cast<int64_t>(v) != p.rows) bad = true;
+        if (i > 0 && p.offsets[i - 1] > v) bad = true;
+      }
+      if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) record_status(p.status, kStatusOffsets);
+    }
+  };
+  if (!kDynamic && gt == 0 && tw == 0) grid_once();
+
+  // Step k uses ring slot k mod S (advanced incrementally); its row comes from the unit held by
+  // lane `slot` (dynamic) or advances by NT (static).
   int slot = 0;
-  uint32_t parity = 0;
-  for (int64_t row = gt; row < p.rows; row += NT, ++k) {
+  int64_t row = gt;
+  for (int64_t k = 0;; ++k) {
+    if constexpr (kDynamic) {
+      const int64_t unit = __shfl_sync(0xFFFFFFFFu, slot_unit, slot);
+      if (unit < 0) break;
+      row = row_of(unit);
+    } else {
+      if (row >= p.rows) break;
+    }
+    if (kDynamic && row == 0 && tw == 0) grid_once();
+    if (row < p.rows) {
     int ok = 1;
-    if (lane == 0 && has_work) ok = mbar_wait_bounded(&my_bars[slot], parity, p.timeout_ns) ? 1 : 0;
+    if (lane == 0 && has_work) {
+      ok = mbar_wait_bounded(&my_bars[slot], (phase >> slot) & 1u, p.timeout_ns) ? 1 : 0;
+      if (ok) {
+        phase ^= 1u << slot;
+        pending &= ~(1u << slot);
+      }
+    }
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     const bool team_sync = !kTensor && TW > 1;
     if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
     if (!ok && !team_sync) {
       // A copy did not land in time: wait for the copies still in flight, and stop.
-      if (lane == 0) drain(k);
+      if (lane == 0) drain();
       return;
     }
     unsigned char* xs = my_ring + static_cast<size_t>(slot) * p.slot_bytes;
@@ -406,9 +539,10 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
           m2 = max_abs_bf16x2(m2, bmax[j]);
         }
       }
-      float a = abs_max_of_pair(m2);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+      // Row amax: the largest BF16 magnitude of the warp (as its bit pattern, which orders like
+      // the magnitude), then the team's.
+      const uint32_t mh = m2 & 0x7FFF7FFFu;
+      float a = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, max(mh >> 16, mh & 0xFFFFu)) << 16);
       if (team_sync) {
         float* part = xch + (k & 1) * kMaxWarpsPerCta;
         if (lane == 0) {
@@ -417,7 +551,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
         }
         named_barrier(1 + team, TW * 32);
         if (abort_flag[team]) {
-          if (lane == 0) drain(k);
+          if (lane == 0) drain();
           return;
         }
         a = 0.0f;
@@ -485,9 +619,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
 
     if (kResidual) {
       // Pass 3: the residual's own per-token scale, then its blocks.
-      float a = abs_max_of_pair(rm2);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+      const uint32_t rh = rm2 & 0x7FFF7FFFu;
+      float a = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, max(rh >> 16, rh & 0xFFFFu)) << 16);
       if (TW > 1) {
         float* part = xch + (2 + (k & 1)) * kMaxWarpsPerCta;
         if (lane == 0) part[warp] = a;
@@ -512,17 +645,24 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
       fence_proxy_async_smem();  // the residual writes above precede the slot's next bulk copy
     }
 
+    }  // row < p.rows
+
     // Slot consumed: refill it with this warp's part of the row `stages` steps ahead.
     __syncwarp();
-    if (lane == 0 && has_work) {
-      const int64_t next = row + static_cast<int64_t>(S) * NT;
-      if (next < p.rows) issue(slot, next);
+    int64_t next;
+    if constexpr (kDynamic) {
+      last = next_unit(last);
+      if (lane == slot) slot_unit = last;
+      next = row_of(last);
+    } else {
+      next = row + static_cast<int64_t>(S) * NT;
+      row += NT;
     }
-    if (++slot == S) {
-      slot = 0;
-      parity ^= 1u;
-    }
+    if (lane == 0 && has_work && next < p.rows) issue(slot, next);
+    if (++slot == S) slot = 0;
   }
+  // Every request thread 0 issued has been answered: the warps read them all up to the first
+  // failure, which is the last one issued.
 }
 
 constexpr int kGuidedUnroll = 4;  // 8-element groups per lane per step of the guided encoder
@@ -710,7 +850,6 @@ bool choose_ring(int64_t cols, RingShape* out, int warps_cap = 0) {
   while (team > 1 && (team - 1) * ((nblk + team - 1) / team) >= nblk) team /= 2;
   const int bpw = (nblk + team - 1) / team;
   const uint32_t slot = static_cast<uint32_t>(((bpw * 32 + 127) / 128) * 128);
-  const size_t avail = kSmemLimit - kHeaderBytes;
   const LaunchOverride ov = launch_override();
   int max_warps = kMaxWarpsPerCta;
   if (ov.warps_per_cta > 0) max_warps = ov.warps_per_cta < team ? team : ov.warps_per_cta;
@@ -720,13 +859,15 @@ bool choose_ring(int64_t cols, RingShape* out, int warps_cap = 0) {
     for (int warps = max_warps; warps >= team; warps -= team) {
       for (int stages = kMaxStages; stages >= min_stages; --stages) {
         if (ov.stages > 0 && stages != ov.stages) continue;
-        if (static_cast<size_t>(warps) * stages * slot > avail) continue;
+        const size_t smem = static_cast<size_t>(ring_header_bytes(warps, stages)) +
+                            static_cast<size_t>(warps) * stages * slot;
+        if (smem > kSmemLimit) continue;
         out->warps = warps;
         out->stages = stages;
         out->team = team;
         out->blocks_per_warp = bpw;
         out->slot_bytes = slot;
-        out->smem = kHeaderBytes + static_cast<size_t>(warps) * stages * slot;
+        out->smem = smem;
         return true;
       }
     }
@@ -773,35 +914,43 @@ cudaError_t launch_impl(QuantParams p, cudaStream_t stream, bool after_amax_kern
     if (err != cudaSuccess) return err;
     if (cached_dev) cache.attr_set[device].store(1);
   }
-  const long long key = static_cast<long long>(rs.warps) | (static_cast<long long>(rs.stages) << 8) |
-                        (static_cast<long long>(rs.slot_bytes) << 16);
-  int per_sm = 0;
-  if (cached_dev)
-    for (auto& e : cache.entries[device])
-      if (e.key.load() == key) {
-        per_sm = e.per_sm.load();
-        break;
-      }
-  if (per_sm == 0) {
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, rs.warps * 32, rs.smem);
-    if (err != cudaSuccess) return err;
-    if (per_sm < 1) per_sm = 1;
-    if (cached_dev)
-      for (auto& e : cache.entries[device]) {
-        long long empty = 0;
-        if (e.key.load() == key) break;
-        if (e.key.compare_exchange_strong(empty, key)) {
-          e.per_sm.store(per_sm);
-          break;
-        }
-      }
-  }
+  // Dynamic schedule (fused): one CTA per work unit (a row per team); the hardware starts as many
+  // as fit and the running ones take over the rest as they free up.  A launch-shape override (or
+  // more units than a grid holds) caps the grid, and each CTA then walks every gridDim.x-th unit
+  // from its own.  Static schedule: one wave of resident CTAs.
   const int teams = rs.warps / rs.team;
   int64_t grid = (p.rows + teams - 1) / teams;
-  const int64_t cap = static_cast<int64_t>(sm_count(device)) * per_sm;
-  if (grid > cap) grid = cap;
+  if (!kFused) {
+    const long long key = static_cast<long long>(rs.warps) |
+                          (static_cast<long long>(rs.stages) << 8) |
+                          (static_cast<long long>(rs.slot_bytes) << 16);
+    int per_sm = 0;
+    if (cached_dev)
+      for (auto& e : cache.entries[device])
+        if (e.key.load() == key) {
+          per_sm = e.per_sm.load();
+          break;
+        }
+    if (per_sm == 0) {
+      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, rs.warps * 32, rs.smem);
+      if (err != cudaSuccess) return err;
+      if (per_sm < 1) per_sm = 1;
+      if (cached_dev)
+        for (auto& e : cache.entries[device]) {
+          long long empty = 0;
+          if (e.key.load() == key) break;
+          if (e.key.compare_exchange_strong(empty, key)) {
+            e.per_sm.store(per_sm);
+            break;
+          }
+        }
+    }
+    const int64_t cap = static_cast<int64_t>(sm_count(device)) * per_sm;
+    if (grid > cap) grid = cap;
+  }
   const LaunchOverride ov = launch_override();
   if (ov.max_ctas > 0 && grid > ov.max_ctas) grid = ov.max_ctas;
+  if (grid > 0x7FFFFFFF) grid = 0x7FFFFFFF;
   if (grid < 1) grid = 1;
   p.stages = rs.stages;
   p.team = rs.team;

@@ -5,7 +5,8 @@ GIL).  Every row of moe_activation (16384x7168), expert_grouped (~32853x7168, wi
 offsets) and long_rollout (131072x7168) is compared bit for bit -- codes, E4M3 block scales, FP32
 row scales and dequantized BF16 -- with the library in its default launch configuration (the one
 the benchmark times).  moe_activation is also checked in mode six, with the FP16 selector, for the
-ResQ residual and for TRACE guidance.
+ResQ residual and for TRACE guidance, and the fused round trip's work-unit hand-over on a
+3653-row instance under several grid caps.
 """
 import os
 from concurrent.futures import ThreadPoolExecutor
@@ -107,6 +108,28 @@ def test_moe_activation_fused_roundtrip_every_row():
     assert_same(_np(scales), want["scales"], "block scales")
     assert_same(_np(sdec), want["scale"], "row scale")
     assert_same(_u16(y), want["y"], "y")
+    assert nv.nvfp4_get_device_status() == 0
+
+
+def test_fused_work_units_taken_over_every_row():
+    """The fused round trip's dynamic schedule: one CTA per work unit (a row for each team of a
+    CTA), and running CTAs take over the units of CTAs that have not started; under a grid cap each
+    CTA walks every cap-th unit and takes over whole walks.  3653 rows: the units outnumber one
+    wave of resident CTAs three times over and the last unit is partial; caps just above one wave,
+    between one and two, and at two waves.  Every row, every cap, against the same oracle result."""
+    rows = 8 * 152 * 3 + 5
+    x = synth.generate(2, device=DEV, rows=rows)["x"]
+    want = oracle_quantize_rows(_u16(x), "four_over_six", want_y=True)
+    try:
+        for cap in (0, 153, 200, 304):
+            nv.nvfp4_set_launch_config(0, 0, cap)
+            codes, scales, sdec, y = nv.nvfp4_fused_roundtrip(x, "row", "four_over_six")
+            assert_same(_np(codes), want["codes"], f"codes (cap {cap})")
+            assert_same(_np(scales), want["scales"], f"block scales (cap {cap})")
+            assert_same(_np(sdec), want["scale"], f"row scale (cap {cap})")
+            assert_same(_u16(y), want["y"], f"y (cap {cap})")
+    finally:
+        nv.nvfp4_set_launch_config(0, 0, 0)
     assert nv.nvfp4_get_device_status() == 0
 
 

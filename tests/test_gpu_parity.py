@@ -296,12 +296,32 @@ def test_bounded_wait_reports_timeout():
 
 @pytest.mark.parametrize("cols,op", [(7168, "rowwise"), (7168, "fused"), (7168, "tensor"),
                                      (7168, "residual"), (2048, "rowwise"), (32768, "rowwise"),
-                                     (65536, "rowwise")])
+                                     (65536, "rowwise"), (7168, "fused_units")])
 def test_quantize_ring_timeout_path(cols, op):
     """The quantize kernel's own failure branches: with one row's copies withheld, the warps that
     own it give up after 1 ms, record NVFP4_ERR_TIMEOUT, drain their copies still in flight and
     return (a team of several warps -- 2 for 7168-wide rows, 8 for 32768, 16 for 65536 -- leaves
-    together behind its barrier); the next ordinary call on the same context is bit-exact."""
+    together behind its barrier); the next ordinary call on the same context is bit-exact.
+    fused_units: 2435 rows, so the withheld row sits in a work unit that a running CTA took over
+    from one that had not started, and the CTAs still waiting for work-unit answers after the
+    failing team left give up in bounded time too; the next call matches a clean call before it
+    (whose rows the other tests check against the oracle)."""
+    if op == "fused_units":
+        x = synth.generate(2, device=DEV, rows=8 * 152 * 2 + 3)["x"]
+        base = [t.clone() for t in nv.nvfp4_fused_roundtrip(x, "row")]
+        nv.nvfp4_get_device_status(clear=True)
+        nv.nvfp4_selftest_withhold_row(2000, 1_000_000)
+        try:
+            nv.nvfp4_fused_roundtrip(x, "row")
+            torch.cuda.synchronize()
+        finally:
+            nv.nvfp4_selftest_withhold_row(-1, 0)
+        assert nv.nvfp4_get_device_status(clear=True) == 5  # NVFP4_ERR_TIMEOUT
+        again = nv.nvfp4_fused_roundtrip(x, "row")
+        for a, b in zip(base, again):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+        assert nv.nvfp4_get_device_status() == 0
+        return
     if cols == 2048:
         x = synth.generate(0, device=DEV, rows=96)["x"]
     elif cols == 7168:
