@@ -577,7 +577,7 @@ def _gemm_check(got, X, W, k):
 
 
 @pytest.mark.parametrize("m,n,k", [(128, 128, 256), (256, 256, 2048), (300, 144, 320),
-                                   (512, 384, 7168)])
+                                   (512, 384, 7168), (640, 272, 768)])
 def test_gemm_nt_matches_float64_product(m, n, k):
     """y = x . Q(w) on the tensor cores against the float64 product of the exactly dequantized
     operands (decoded independently of the library).  Both operands are quantized by the oracle;
