@@ -3,13 +3,15 @@
 // codes, and optionally the BF16 dequantized round trip (Sec. 3) in the same pass.
 //
 // Shape of the computation.  Every element is read once (2 B) and written once (0.5625 B, plus
-// 2 B for the round trip).  A persistent grid (one CTA of 16 warps per SM) walks the rows in
-// teams of warps that share a row, each warp owning a contiguous part of it.  Each warp owns a
-// ring of shared-memory slots, one part-row per slot, filled by bulk asynchronous copies
-// (cp.async.bulk, the non-tensor TMA path) that complete on per-slot mbarriers: while the warp
-// encodes row k, its parts of the next rows are in flight.  Per row:
-//   pass 1  row amax from shared memory (packed BF16x2 |max|, warp shuffle, then the team's
-//           partial maxima through shared memory);
+// 2 B for the round trip).  CTAs of 16 warps, one per SM, walk the rows in teams of warps that
+// share a row, each warp owning a contiguous part of it: the issue-bound quantize-only kernels in
+// one static wave, the HBM-bound round trip in work units that running CTAs take over from CTAs
+// not yet started (cluster launch control), in order.  Each warp owns a ring of shared-memory
+// slots, one part-row per slot, filled by bulk asynchronous copies (cp.async.bulk, the non-tensor
+// TMA path) that complete on per-slot mbarriers: while the warp encodes row k, its parts of the
+// next rows are in flight.  Per row:
+//   pass 1  row amax from shared memory (packed BF16x2 |max|, one redux over the warp, then the
+//           team's partial maxima through shared memory);
 //   pass 2  one lane per 16-element block: block amax, both candidate E4M3 scales, E2M1 codes
 //           for both candidates, their block squared errors, the 4/6 choice, and the stores.
 // Each launch is a programmatic dependent of the previous kernel on the stream: shared-memory
