@@ -272,9 +272,9 @@ nvfp4_status nvfp4_set_launch_config(int warps_per_cta, int stages, int max_ctas
 nvfp4_status nvfp4_selftest_wait_timeout(uint64_t timeout_ns, nvfp4_stream_t stream);
 
 /* Self-test of the quantize kernels' own failure path.  Until it is called again with row = -1,
- * every quantize call (row or tensor scale, plain, fused or residual) withholds the
- * shared-memory copies of row `row` of its input: the warps that own that row wait on their ring
- * barrier in vain, give up after timeout_ns nanoseconds, record NVFP4_ERR_TIMEOUT in the device
+ * every quantize call (row or tensor scale, plain, fused or residual) and every guided call whose
+ * rows are staged through shared memory (cols a multiple of 1024) withholds the shared-memory
+ * copies of row `row` of its input: the warps that own that row wait on their ring barrier in vain, give up after timeout_ns nanoseconds, record NVFP4_ERR_TIMEOUT in the device
  * status word, wait (within the library's usual 4 s bound) for their other copies still in
  * flight, and return, leaving their remaining rows unwritten; warps sharing a row leave together.
  * Every other wait keeps working, so every launch ends.  timeout_ns must be in (0, 4e9] when

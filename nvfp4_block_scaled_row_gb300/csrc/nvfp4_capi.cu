@@ -240,8 +240,12 @@ nvfp4_status nvfp4_quantize_guided(const void* x, int64_t rows, int64_t cols, nv
   if (overlap(codes, n / 2, x, 2 * n) || overlap(codes, n / 2, row_amax, 4 * static_cast<size_t>(rows)) ||
       overlap(codes, n / 2, ref_codes, n / 2) || overlap(codes, n / 2, ref_block_scales, n / 16))
     return NVFP4_ERR_INVALID_ARG;
+  int* status = nullptr;
+  if (device_status_word(&status) != cudaSuccess) return NVFP4_ERR_CUDA;
   GuidedParams p{static_cast<const uint16_t*>(x), rows, static_cast<int32_t>(cols), row_amax,
-                 ref_codes, ref_block_scales, codes};
+                 ref_codes, ref_block_scales, codes, status, kWaitTimeoutNs, kWaitTimeoutNs,
+                 static_cast<int64_t>(g_withhold_row.load())};
+  if (p.withhold_row >= 0) p.timeout_ns = g_withhold_timeout_ns.load();
   return from_cuda(launch_quantize_guided(mode, p, reinterpret_cast<cudaStream_t>(stream)));
 }
 

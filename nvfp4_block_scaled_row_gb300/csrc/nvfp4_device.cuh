@@ -84,6 +84,10 @@ struct GuidedParams {
   const uint8_t* ref_codes;   // the rollout's codes [rows][cols/2]
   const uint8_t* ref_scales;  // the rollout's E4M3 block scales [rows][cols/16]
   uint8_t* codes;             // output codes [rows][cols/2]
+  int* status;                // device status word
+  uint64_t timeout_ns;        // bound on every ring-slot wait (ring variant)
+  uint64_t drain_timeout_ns;  // bound on each wait for a copy still in flight before an early exit
+  int64_t withhold_row;       // self-test only: the row whose copies are never issued (-1: none)
 };
 
 struct DequantParams {

@@ -700,6 +700,47 @@ __device__ __forceinline__ uint32_t sign_nibbles(const float (&v)[8]) {
 // Magnitude comparisons of the rollout's codes R with m use borrow-free nibble subtraction
 // ((R | 8) - m keeps bit 3 exactly when R >= m).  The magnitude then moves by -1 (away, unless the
 // rollout's code is on the same side with R >= m) or +1 (towards, when it is with R > m).
+// One 8-element group of the guided encoder: xw = the trainer's eight BF16 values, ref = the
+// rollout's eight codes (element i in nibble i), e = the rollout's block scale.  Returns the
+// eight output codes.
+__device__ __forceinline__ uint32_t guided_group(const uint4 xw, uint32_t ref, const ScaleEntry e,
+                                                 f32x2 senc2) {
+  const uint32_t one_h2 = 0x3C003C00u;   // FP16 (1, 1)
+  const uint32_t mone_h2 = 0xBC00BC00u;  // FP16 (-1, -1)
+  const f32x2 inv2 = pack2(e.inv, e.inv);
+  const f32x2 ninv2 = pack2(-e.inv, -e.inv);
+  f32x2 z[4], t[4];
+  z[0] = mul2(bf16x2_to_f32x2(xw.x), senc2);
+  z[1] = mul2(bf16x2_to_f32x2(xw.y), senc2);
+  z[2] = mul2(bf16x2_to_f32x2(xw.z), senc2);
+  z[3] = mul2(bf16x2_to_f32x2(xw.w), senc2);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) t[j] = mul2(z[j], inv2);
+  uint32_t r[4];
+  const uint32_t rtn = e2m1x8_encode_decode(t[0], t[1], t[2], t[3], r);
+  float uu[8], vv[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const f32x2 nt = mul2(z[j], ninv2);                     // -t, exactly
+    const f32x2 uj = fma_f16x2_f32x2(r[j], one_h2, nt);     // r - t, one rounding
+    const f32x2 vj = fma_f16x2_f32x2(r[j], mone_h2, t[j]);  // t - r, one rounding
+    unpack2(uj, uu[2 * j], uu[2 * j + 1]);
+    unpack2(vj, vv[2 * j], vv[2 * j + 1]);
+  }
+  const uint32_t su = sign_nibbles(uu), sv = sign_nibbles(vv);
+  const uint32_t st = rtn & 0x88888888u;                        // sign of t (bit 3)
+  const uint32_t away = (st & su) | (~st & sv);                 // bit 3 meaningful
+  const uint32_t toward = (st & sv) | (~st & su);
+  const uint32_t mag = rtn & 0x77777777u;
+  const uint32_t rg = ref | 0x88888888u;
+  const uint32_t ge = rg - mag;                                 // bit 3: R >= m
+  const uint32_t gt = rg - mag - 0x11111111u;                   // bit 3: R > m
+  const uint32_t other = rtn ^ ref;                             // bit 3: R on the other side
+  const uint32_t down = away & (~ge | other) & 0x88888888u;
+  const uint32_t up = toward & gt & ~other & 0x88888888u;
+  return rtn + (up >> 3) - (down >> 3);
+}
+
 template <int kMode>
 __global__ void __launch_bounds__(256) guided_kernel(const GuidedParams p) {
   __shared__ ScaleEntry tab[256];
@@ -710,8 +751,6 @@ __global__ void __launch_bounds__(256) guided_kernel(const GuidedParams p) {
   const int64_t NW = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int cols = p.cols;
   const int ngroups = cols / 8;
-  const uint32_t one_h2 = 0x3C003C00u;   // FP16 (1, 1)
-  const uint32_t mone_h2 = 0xBC00BC00u;  // FP16 (-1, -1)
   // Work units: kGuidedUnroll * 32 consecutive 8-element groups of one row, so a lane has
   // kGuidedUnroll independent loads in flight.  Each warp takes a contiguous range of units (the
   // row factors are recomputed only when the row changes), which balances rows across warps.
@@ -762,39 +801,135 @@ __global__ void __launch_bounds__(256) guided_kernel(const GuidedParams p) {
     for (int k = 0; k < kGuidedUnroll; ++k) {
       const int g = g0 + 32 * k;
       if (g >= ngroups) break;
-      const ScaleEntry e = tab[sb[k]];
-      const f32x2 inv2 = pack2(e.inv, e.inv);
-      const f32x2 ninv2 = pack2(-e.inv, -e.inv);
-      f32x2 z[4], t[4];
-      z[0] = mul2(bf16x2_to_f32x2(xw[k].x), senc2);
-      z[1] = mul2(bf16x2_to_f32x2(xw[k].y), senc2);
-      z[2] = mul2(bf16x2_to_f32x2(xw[k].z), senc2);
-      z[3] = mul2(bf16x2_to_f32x2(xw[k].w), senc2);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) t[j] = mul2(z[j], inv2);
-      uint32_t r[4];
-      const uint32_t rtn = e2m1x8_encode_decode(t[0], t[1], t[2], t[3], r);
-      float uu[8], vv[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const f32x2 nt = mul2(z[j], ninv2);                     // -t, exactly
-        const f32x2 uj = fma_f16x2_f32x2(r[j], one_h2, nt);     // r - t, one rounding
-        const f32x2 vj = fma_f16x2_f32x2(r[j], mone_h2, t[j]);  // t - r, one rounding
-        unpack2(uj, uu[2 * j], uu[2 * j + 1]);
-        unpack2(vj, vv[2 * j], vv[2 * j + 1]);
+      __stcs(out + g, guided_group(xw[k], ref[k], tab[sb[k]], senc2));
+    }
+  }
+}
+
+// The guided encoder with its inputs staged through shared memory: rows whose width is a multiple
+// of kGuidedChunk (and 16-byte aligned tensors).  Work unit = one kGuidedChunk-element piece of a
+// row: its BF16 values, the rollout's codes and block scales, moved by three bulk copies into
+// one slot of the warp's ring (completing on the slot's mbarrier), so each warp keeps
+// kGuidedStages units of loads in flight instead of one per lane.  Lane l then encodes groups
+// l, l + 32, ... of the unit from shared memory exactly as guided_kernel does.
+constexpr int kGuidedChunk = 32 * kGuidedUnroll * 8;                  // 1024 elements
+constexpr int kGuidedXBytes = kGuidedChunk * 2;
+constexpr int kGuidedCodeBytes = kGuidedChunk / 2;
+constexpr int kGuidedScaleBytes = kGuidedChunk / kBlockElems;
+constexpr int kGuidedSlotBytes =
+    ((kGuidedXBytes + kGuidedCodeBytes + kGuidedScaleBytes + 127) / 128) * 128;
+constexpr int kGuidedStages = 4;
+constexpr int kGuidedWarps = 16;
+constexpr int kGuidedBarBytes = ((kGuidedWarps * kGuidedStages * 8 + 127) / 128) * 128;
+constexpr size_t kGuidedSmem = kTableBytes + kGuidedBarBytes +
+                               static_cast<size_t>(kGuidedWarps) * kGuidedStages * kGuidedSlotBytes;
+
+template <int kMode>
+__global__ void __launch_bounds__(kGuidedWarps * 32, 1) guided_ring_kernel(const GuidedParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  ScaleEntry* tab = reinterpret_cast<ScaleEntry*>(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTableBytes);
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  uint64_t* my_bars = bars + warp * kGuidedStages;
+  unsigned char* my_ring = smem + kTableBytes + kGuidedBarBytes +
+                           static_cast<size_t>(warp) * kGuidedStages * kGuidedSlotBytes;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) tab[i] = make_scale_entry(i);
+  if (lane == 0)
+    for (int s = 0; s < kGuidedStages; ++s) mbar_init(&my_bars[s], 1);
+  fence_barrier_init();
+  __syncthreads();
+
+  const int cols = p.cols;
+  const int upr = cols / kGuidedChunk;  // units per row
+  const int64_t total = p.rows * upr;
+  const int64_t NW = static_cast<int64_t>(gridDim.x) * nwarps;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
+  const int64_t per_warp = (total + NW - 1) / NW;
+  const int64_t u_begin = min(total, gw * per_warp);
+  const int64_t u_end = min(total, u_begin + per_warp);
+  const uint64_t policy = l2_evict_first_policy();
+
+  // Copy cursor (lane 0): the row and chunk of the next unit to copy, walked without divisions.
+  int64_t c_row = u_begin / upr;
+  int c_chunk = static_cast<int>(u_begin - c_row * upr);
+  int64_t copied = u_begin;
+  uint32_t pending = 0, phase = 0;
+  if (lane == 0 && u_begin < u_end)  // the first unit's values into L2 while the wait runs
+    bulk_prefetch_l2(p.x + c_row * cols + c_chunk * kGuidedChunk, kGuidedXBytes);
+  pdl_wait();  // global memory only after the previous kernel on the stream
+  pdl_trigger();
+  // (The self-test's withheld row is never copied, so the wait for its units runs out.)
+  auto issue = [&](int slot) {
+    if (c_row != p.withhold_row) {
+      unsigned char* dst = my_ring + slot * kGuidedSlotBytes;
+      const int64_t e0 = c_row * cols + static_cast<int64_t>(c_chunk) * kGuidedChunk;
+      mbar_arrive_expect_tx(&my_bars[slot], kGuidedXBytes + kGuidedCodeBytes + kGuidedScaleBytes);
+      bulk_load(dst, p.x + e0, kGuidedXBytes, &my_bars[slot], policy);
+      bulk_load(dst + kGuidedXBytes, p.ref_codes + e0 / 2, kGuidedCodeBytes, &my_bars[slot],
+                policy);
+      bulk_load(dst + kGuidedXBytes + kGuidedCodeBytes, p.ref_scales + e0 / kBlockElems,
+                kGuidedScaleBytes, &my_bars[slot], policy);
+      pending |= 1u << slot;
+    }
+    ++copied;
+    if (++c_chunk == upr) {
+      c_chunk = 0;
+      ++c_row;
+    }
+  };
+  if (lane == 0)
+    for (int s = 0; s < kGuidedStages && copied < u_end; ++s) issue(s);
+
+  int64_t row = u_begin / upr;
+  int chunk = static_cast<int>(u_begin - row * upr);
+  int64_t cur_row = -1;
+  f32x2 senc2 = pack2(0.0f, 0.0f);
+  int slot = 0;
+  for (int64_t u = u_begin; u < u_end; ++u) {
+    int ok = 1;
+    if (lane == 0) {
+      ok = mbar_wait_bounded(&my_bars[slot], (phase >> slot) & 1u, p.timeout_ns) ? 1 : 0;
+      if (ok) {
+        phase ^= 1u << slot;
+        pending &= ~(1u << slot);
       }
-      const uint32_t su = sign_nibbles(uu), sv = sign_nibbles(vv);
-      const uint32_t st = rtn & 0x88888888u;                        // sign of t (bit 3)
-      const uint32_t away = (st & su) | (~st & sv);                 // bit 3 meaningful
-      const uint32_t toward = (st & sv) | (~st & su);
-      const uint32_t mag = rtn & 0x77777777u;
-      const uint32_t rg = ref[k] | 0x88888888u;
-      const uint32_t ge = rg - mag;                                 // bit 3: R >= m
-      const uint32_t gt = rg - mag - 0x11111111u;                   // bit 3: R > m
-      const uint32_t other = rtn ^ ref[k];                          // bit 3: R on the other side
-      const uint32_t down = away & (~ge | other) & 0x88888888u;
-      const uint32_t up = toward & gt & ~other & 0x88888888u;
-      __stcs(out + g, rtn + (up >> 3) - (down >> 3));
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) {
+      // A copy did not land in time: wait (bounded) for the copies still in flight, and stop.
+      if (lane == 0) {
+        record_status(p.status, kStatusTimeout);
+        for (int s = 0; s < kGuidedStages; ++s)
+          if ((pending >> s) & 1u)
+            (void)mbar_wait_bounded(&my_bars[s], (phase >> s) & 1u, p.drain_timeout_ns);
+      }
+      return;
+    }
+    if (row != cur_row) {
+      const RowFactors f = row_factors_warp<kMode>(p.row_amax[row], lane);
+      senc2 = pack2(f.S_enc, f.S_enc);
+      cur_row = row;
+    }
+    const unsigned char* xs = my_ring + slot * kGuidedSlotBytes;
+    uint32_t* out = reinterpret_cast<uint32_t*>(p.codes + row * (cols / 2)) +
+                    chunk * (kGuidedChunk / 8);
+#pragma unroll
+    for (int k = 0; k < kGuidedUnroll; ++k) {
+      const int g = lane + 32 * k;  // 8-element group of the unit
+      const uint4 xw = *reinterpret_cast<const uint4*>(xs + g * 16);
+      const uint32_t ref = *reinterpret_cast<const uint32_t*>(xs + kGuidedXBytes + g * 4);
+      const uint32_t sb = xs[kGuidedXBytes + kGuidedCodeBytes + (g >> 1)];
+      __stcs(out + g, guided_group(xw, ref, tab[sb], senc2));
+    }
+    // Slot consumed: refill it with this warp's unit kGuidedStages ahead.
+    __syncwarp();
+    if (lane == 0 && copied < u_end) issue(slot);
+    if (++slot == kGuidedStages) slot = 0;
+    if (++chunk == upr) {
+      chunk = 0;
+      ++row;
     }
   }
 }
@@ -1023,6 +1158,36 @@ cudaError_t launch_quantize_guided(int mode, const GuidedParams& p, cudaStream_t
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
+  // Rows that split into whole units over 16-byte aligned tensors go through the staged ring.
+  const bool ring = p.cols % kGuidedChunk == 0 &&
+                    (reinterpret_cast<uintptr_t>(p.x) | reinterpret_cast<uintptr_t>(p.ref_codes) |
+                     reinterpret_cast<uintptr_t>(p.ref_scales)) % 16 == 0;
+  if (ring) {
+    auto rkern = mode == kModeSix ? guided_ring_kernel<kModeSix>
+                                  : guided_ring_kernel<kModeFourOverSix>;
+    static std::atomic<int> attr_set[64];
+    const bool cached_dev = device >= 0 && device < 64;
+    if (!cached_dev || attr_set[device].load() == 0) {
+      err = cudaFuncSetAttribute(guided_ring_kernel<kModeSix>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kGuidedSmem));
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(guided_ring_kernel<kModeFourOverSix>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(kGuidedSmem));
+      if (err != cudaSuccess) return err;
+      if (cached_dev) attr_set[device].store(1);
+    }
+    const int64_t units = p.rows * (p.cols / kGuidedChunk);
+    int64_t grid = (units + kGuidedWarps - 1) / kGuidedWarps;
+    const int64_t cap = sm_count(device);
+    if (grid > cap) grid = cap;
+    const LaunchOverride ov = launch_override();
+    if (ov.max_ctas > 0 && grid > ov.max_ctas) grid = ov.max_ctas;
+    if (grid < 1) grid = 1;
+    return launch_programmatic(rkern, dim3(static_cast<unsigned>(grid)), dim3(kGuidedWarps * 32),
+                               kGuidedSmem, stream, p);
+  }
   // The guided encoder keeps the rollout's scales: only M (mode six or not) matters.
   auto kern = mode == kModeSix ? guided_kernel<kModeSix> : guided_kernel<kModeFourOverSix>;
   // One wave of resident blocks; the kernel spreads the work units over its warps.

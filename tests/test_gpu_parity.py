@@ -505,6 +505,27 @@ def test_guided_rounding_matches_oracle(index, rows):
     assert nv.nvfp4_get_device_status() == 0
 
 
+def test_guided_ring_timeout_path():
+    """The staged guided encoder's failure branch: with one row's copies withheld, the warp whose
+    units include it gives up after 1 ms, records NVFP4_ERR_TIMEOUT, drains its copies still in
+    flight and returns; the next ordinary call on the same context matches the oracle."""
+    x_roll = synth.generate(2, device=DEV, rows=96)["x"]
+    (amax_h, codes_h, scales_h), (amax, codes, scales) = _oracle_record(x_roll)
+    x_tr = _perturbed(x_roll, 2)
+    nv.nvfp4_get_device_status(clear=True)
+    nv.nvfp4_selftest_withhold_row(5, 1_000_000)
+    try:
+        nv.nvfp4_quantize_guided(x_tr, amax, codes, scales)
+        torch.cuda.synchronize()
+    finally:
+        nv.nvfp4_selftest_withhold_row(-1, 0)
+    assert nv.nvfp4_get_device_status(clear=True) == 5  # NVFP4_ERR_TIMEOUT
+    got = nv.nvfp4_quantize_guided(x_tr, amax, codes, scales)
+    want = oracle.quantize_guided(synth.as_u16(x_tr), amax_h, codes_h, scales_h)
+    _assert_equal(_np(got), want, "guided codes after the timeout")
+    assert nv.nvfp4_get_device_status() == 0
+
+
 @pytest.mark.parametrize("cols", [16, 48, 7184])
 def test_guided_rounding_edge_values(cols):
     x_roll = _edge_matrix(16, cols, seed=cols + 3)
