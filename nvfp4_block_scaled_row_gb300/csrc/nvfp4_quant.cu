@@ -507,145 +507,149 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1) quantize_kernel(const
     }
     if (kDynamic && row == 0 && tw == 0) grid_once();
     if (row < p.rows) {
-    int ok = 1;
-    if (lane == 0 && has_work) {
-      ok = mbar_wait_bounded(&my_bars[slot], (phase >> slot) & 1u, p.timeout_ns) ? 1 : 0;
-      if (ok) {
-        phase ^= 1u << slot;
-        pending &= ~(1u << slot);
+      int ok = 1;
+      if (lane == 0 && has_work) {
+        ok = mbar_wait_bounded(&my_bars[slot], (phase >> slot) & 1u, p.timeout_ns) ? 1 : 0;
+        if (ok) {
+          phase ^= 1u << slot;
+          pending &= ~(1u << slot);
+        }
       }
-    }
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    const bool team_sync = !kTensor && TW > 1;
-    if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
-    if (!ok && !team_sync) {
-      // A copy did not land in time: wait for the copies still in flight, and stop.
-      if (lane == 0) drain();
-      return;
-    }
-    unsigned char* xs = my_ring + static_cast<size_t>(slot) * p.slot_bytes;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      const bool team_sync = !kTensor && TW > 1;
+      if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
+      if (!ok && !team_sync) {
+        // A copy did not land in time: wait for the copies still in flight, and stop.
+        if (lane == 0) drain();
+        return;
+      }
+      unsigned char* xs = my_ring + static_cast<size_t>(slot) * p.slot_bytes;
 
-    // Pass 1 (row scale): block maxima (kept in registers for pass 2) and the row amax.
-    uint32_t bmax[kMaxBlocksPerLane];
-    if (!kTensor) {
-      uint32_t m2 = 0;
+      // Pass 1 (row scale): block maxima (kept in registers for pass 2) and the row amax.
+      uint32_t bmax[kMaxBlocksPerLane];
+      if (!kTensor) {
+        uint32_t m2 = 0;
 #pragma unroll
-      for (int j = 0; j < kMaxBlocksPerLane; ++j) {
-        const int b = b0 + lane + 32 * j;
-        bmax[j] = 0;
-        if ((kNB > 0 && !kResidual) ? j < kNB : (ok && b < b1)) {
+        for (int j = 0; j < kMaxBlocksPerLane; ++j) {
+          const int b = b0 + lane + 32 * j;
+          bmax[j] = 0;
+          if ((kNB > 0 && !kResidual) ? j < kNB : (ok && b < b1)) {
+            const unsigned char* blk = xs + (b - b0) * 32;
+            const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
+            const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
+            bmax[j] = block_max_word(A, B);
+            m2 = max_abs_bf16x2(m2, bmax[j]);
+          }
+        }
+        // Row amax: the largest BF16 magnitude of the warp (as its bit pattern, which orders like
+        // the magnitude), then the team's.
+        const uint32_t mh = m2 & 0x7FFF7FFFu;
+        const uint32_t mtop = __reduce_max_sync(0xFFFFFFFFu, max(mh >> 16, mh & 0xFFFFu));
+        float a = __uint_as_float(mtop << 16);
+        if (team_sync) {
+          float* part = xch + (k & 1) * kMaxWarpsPerCta;
+          if (lane == 0) {
+            part[warp] = a;
+            if (!ok) abort_flag[team] = 1;
+          }
+          named_barrier(1 + team, TW * 32);
+          if (abort_flag[team]) {
+            if (lane == 0) drain();
+            return;
+          }
+          a = 0.0f;
+          for (int j = 0; j < TW; ++j) a = fmaxf(a, part[team * TW + j]);
+        }
+        f = row_factors_warp<kMode>(a, lane);
+        if (lane == 0 && tw == 0) p.scale_out[row] = f.S_dec;
+      }
+
+      // Pass 2: encode this warp's blocks (residual kernels also turn each block into its BF16
+      // residual x - DQ(Q(x)) in place, with the residual's block maxima kept for pass 3).
+      uint8_t* codes_row = p.codes + row * (cols / 2);
+      uint8_t* scales_row = p.scales + row * nblk;
+      uint32_t rmax[kMaxBlocksPerLane];
+      uint32_t rm2 = 0;
+      if (!kResidual && f.S_dec == 0.0f) {
+        // Zero amax (a padding row, or an all-zero tensor): every element is +-0, so every scale
+        // is 0, every code is the sign of its element (0x0 or 0x8) and y = x, bit for bit.
+#pragma unroll
+        for (int j = 0; j < (kNB > 0 ? kNB : kMaxBlocksPerLane); ++j) {
+          const int b = b0 + lane + 32 * j;
+          if (kNB == 0 && b >= b1) break;
           const unsigned char* blk = xs + (b - b0) * 32;
           const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
           const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
-          bmax[j] = block_max_word(A, B);
-          m2 = max_abs_bf16x2(m2, bmax[j]);
+          uint32_t* cw = reinterpret_cast<uint32_t*>(codes_row + b * 8);
+          cw[h0] = sign_codes(A);
+          cw[1 - h0] = sign_codes(B);
+          scales_row[b] = 0;
+          if (kFused) {
+            uint16_t* y_blk = p.y + row * cols + b * kBlockElems;
+            *reinterpret_cast<uint4*>(y_blk + h0 * 8) = A;
+            *reinterpret_cast<uint4*>(y_blk + (1 - h0) * 8) = B;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < ((kNB > 0 && !kResidual) ? kNB : kMaxBlocksPerLane); ++j) {
+          const int b = b0 + lane + 32 * j;
+          if ((kNB == 0 || kResidual) && b >= b1) break;
+          unsigned char* blk = xs + (b - b0) * 32;
+          uint4 lo, hi;
+          load_block<kFused>(blk, lo, hi);
+          const float m = abs_max_word(kTensor ? block_max_word(lo, hi) : bmax[j]);
+          uint32_t out[8];
+          encode_block<kMode, kFused || kResidual>(lo, hi, m, f, tab, codes_row + b * 8,
+                                                   scales_row + b, out);
+          if (kFused) {
+            uint16_t* y_blk = p.y + row * cols + b * kBlockElems;
+            *reinterpret_cast<uint4*>(y_blk) = make_uint4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<uint4*>(y_blk + 8) = make_uint4(out[4], out[5], out[6], out[7]);
+          }
+          if (kResidual) {
+            const uint4 RL =
+                make_uint4(bf16x2_residual(lo.x, out[0]), bf16x2_residual(lo.y, out[1]),
+                           bf16x2_residual(lo.z, out[2]), bf16x2_residual(lo.w, out[3]));
+            const uint4 RH =
+                make_uint4(bf16x2_residual(hi.x, out[4]), bf16x2_residual(hi.y, out[5]),
+                           bf16x2_residual(hi.z, out[6]), bf16x2_residual(hi.w, out[7]));
+            *reinterpret_cast<uint4*>(blk) = RL;
+            *reinterpret_cast<uint4*>(blk + 16) = RH;
+            rmax[j] = block_max_word(RL, RH);
+            rm2 = max_abs_bf16x2(rm2, rmax[j]);
+          }
         }
       }
-      // Row amax: the largest BF16 magnitude of the warp (as its bit pattern, which orders like
-      // the magnitude), then the team's.
-      const uint32_t mh = m2 & 0x7FFF7FFFu;
-      float a = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, max(mh >> 16, mh & 0xFFFFu)) << 16);
-      if (team_sync) {
-        float* part = xch + (k & 1) * kMaxWarpsPerCta;
-        if (lane == 0) {
-          part[warp] = a;
-          if (!ok) abort_flag[team] = 1;
-        }
-        named_barrier(1 + team, TW * 32);
-        if (abort_flag[team]) {
-          if (lane == 0) drain();
-          return;
-        }
-        a = 0.0f;
-        for (int j = 0; j < TW; ++j) a = fmaxf(a, part[team * TW + j]);
-      }
-      f = row_factors_warp<kMode>(a, lane);
-      if (lane == 0 && tw == 0) p.scale_out[row] = f.S_dec;
-    }
 
-    // Pass 2: encode this warp's blocks (residual kernels also turn each block into its BF16
-    // residual x - DQ(Q(x)) in place, with the residual's block maxima kept for pass 3).
-    uint8_t* codes_row = p.codes + row * (cols / 2);
-    uint8_t* scales_row = p.scales + row * nblk;
-    uint32_t rmax[kMaxBlocksPerLane];
-    uint32_t rm2 = 0;
-    if (!kResidual && f.S_dec == 0.0f) {
-      // Zero amax (a padding row, or an all-zero tensor): every element is +-0, so every scale
-      // is 0, every code is the sign of its element (0x0 or 0x8) and y = x, bit for bit.
-#pragma unroll
-      for (int j = 0; j < (kNB > 0 ? kNB : kMaxBlocksPerLane); ++j) {
-        const int b = b0 + lane + 32 * j;
-        if (kNB == 0 && b >= b1) break;
-        const unsigned char* blk = xs + (b - b0) * 32;
-        const uint4 A = *reinterpret_cast<const uint4*>(blk + h0 * 16);
-        const uint4 B = *reinterpret_cast<const uint4*>(blk + (1 - h0) * 16);
-        uint32_t* cw = reinterpret_cast<uint32_t*>(codes_row + b * 8);
-        cw[h0] = sign_codes(A);
-        cw[1 - h0] = sign_codes(B);
-        scales_row[b] = 0;
-        if (kFused) {
-          uint16_t* y_blk = p.y + row * cols + b * kBlockElems;
-          *reinterpret_cast<uint4*>(y_blk + h0 * 8) = A;
-          *reinterpret_cast<uint4*>(y_blk + (1 - h0) * 8) = B;
-        }
-      }
-    } else {
-#pragma unroll
-    for (int j = 0; j < ((kNB > 0 && !kResidual) ? kNB : kMaxBlocksPerLane); ++j) {
-      const int b = b0 + lane + 32 * j;
-      if ((kNB == 0 || kResidual) && b >= b1) break;
-      unsigned char* blk = xs + (b - b0) * 32;
-      uint4 lo, hi;
-      load_block<kFused>(blk, lo, hi);
-      const float m = abs_max_word(kTensor ? block_max_word(lo, hi) : bmax[j]);
-      uint32_t out[8];
-      encode_block<kMode, kFused || kResidual>(lo, hi, m, f, tab, codes_row + b * 8,
-                                               scales_row + b, out);
-      if (kFused) {
-        uint16_t* y_blk = p.y + row * cols + b * kBlockElems;
-        *reinterpret_cast<uint4*>(y_blk) = make_uint4(out[0], out[1], out[2], out[3]);
-        *reinterpret_cast<uint4*>(y_blk + 8) = make_uint4(out[4], out[5], out[6], out[7]);
-      }
       if (kResidual) {
-        const uint4 RL = make_uint4(bf16x2_residual(lo.x, out[0]), bf16x2_residual(lo.y, out[1]),
-                                    bf16x2_residual(lo.z, out[2]), bf16x2_residual(lo.w, out[3]));
-        const uint4 RH = make_uint4(bf16x2_residual(hi.x, out[4]), bf16x2_residual(hi.y, out[5]),
-                                    bf16x2_residual(hi.z, out[6]), bf16x2_residual(hi.w, out[7]));
-        *reinterpret_cast<uint4*>(blk) = RL;
-        *reinterpret_cast<uint4*>(blk + 16) = RH;
-        rmax[j] = block_max_word(RL, RH);
-        rm2 = max_abs_bf16x2(rm2, rmax[j]);
-      }
-    }
-    }
-
-    if (kResidual) {
-      // Pass 3: the residual's own per-token scale, then its blocks.
-      const uint32_t rh = rm2 & 0x7FFF7FFFu;
-      float a = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, max(rh >> 16, rh & 0xFFFFu)) << 16);
-      if (TW > 1) {
-        float* part = xch + (2 + (k & 1)) * kMaxWarpsPerCta;
-        if (lane == 0) part[warp] = a;
-        named_barrier(1 + team, TW * 32);
-        a = 0.0f;
-        for (int j = 0; j < TW; ++j) a = fmaxf(a, part[team * TW + j]);
-      }
-      const RowFactors g = row_factors_warp<kMode>(a, lane);
-      if (lane == 0 && tw == 0) p.res_scale_out[row] = g.S_dec;
-      uint8_t* rcodes_row = p.res_codes + row * (cols / 2);
-      uint8_t* rscales_row = p.res_scales + row * nblk;
+        // Pass 3: the residual's own per-token scale, then its blocks.
+        const uint32_t rh = rm2 & 0x7FFF7FFFu;
+        const uint32_t rtop = __reduce_max_sync(0xFFFFFFFFu, max(rh >> 16, rh & 0xFFFFu));
+        float a = __uint_as_float(rtop << 16);
+        if (TW > 1) {
+          float* part = xch + (2 + (k & 1)) * kMaxWarpsPerCta;
+          if (lane == 0) part[warp] = a;
+          named_barrier(1 + team, TW * 32);
+          a = 0.0f;
+          for (int j = 0; j < TW; ++j) a = fmaxf(a, part[team * TW + j]);
+        }
+        const RowFactors g = row_factors_warp<kMode>(a, lane);
+        if (lane == 0 && tw == 0) p.res_scale_out[row] = g.S_dec;
+        uint8_t* rcodes_row = p.res_codes + row * (cols / 2);
+        uint8_t* rscales_row = p.res_scales + row * nblk;
 #pragma unroll
-      for (int j = 0; j < (kNB > 0 ? kNB : kMaxBlocksPerLane); ++j) {
-        const int b = b0 + lane + 32 * j;
-        if (kNB == 0 && b >= b1) break;
-        uint4 lo, hi;
-        load_block<false>(xs + (b - b0) * 32, lo, hi);
-        uint32_t unused[8];
-        encode_block<kMode, false>(lo, hi, abs_max_word(rmax[j]), g, tab, rcodes_row + b * 8,
-                                   rscales_row + b, unused);
+        for (int j = 0; j < (kNB > 0 ? kNB : kMaxBlocksPerLane); ++j) {
+          const int b = b0 + lane + 32 * j;
+          if (kNB == 0 && b >= b1) break;
+          uint4 lo, hi;
+          load_block<false>(xs + (b - b0) * 32, lo, hi);
+          uint32_t unused[8];
+          encode_block<kMode, false>(lo, hi, abs_max_word(rmax[j]), g, tab, rcodes_row + b * 8,
+                                     rscales_row + b, unused);
+        }
+        fence_proxy_async_smem();  // the residual writes above precede the slot's next bulk copy
       }
-      fence_proxy_async_smem();  // the residual writes above precede the slot's next bulk copy
-    }
 
     }  // row < p.rows
 
