@@ -21,8 +21,10 @@
 //               16 values along K, M = 128, N = 256, K = 64, FP32 accumulation in TMEM), releases
 //               each stage with tcgen05.commit and hands the finished accumulator over;
 //   warps 2-9   epilogue: warp w reads TMEM lanes 32*(w % 4) .. +31 (its 32 rows) and 128 of the
-//               256 accumulator columns with tcgen05.ld and writes
-//               y[m][n] = bf16(fp32(fp32(D[m][n] * S_x[m]) * S_w)) straight to global memory.
+//               256 accumulator columns with tcgen05.ld, forms
+//               y[m][n] = bf16(fp32(fp32(D[m][n] * S_x[m]) * S_w)) in registers, hands the
+//               accumulator back (the next tile's products start), then writes y straight to
+//               global memory.
 // Measured on GB300 (16384 x 2048 x 7168): consecutive products into one accumulator run about
 // 250 cycles apart whatever N is, so each product takes the widest N (256) the accumulator and
 // the scale slots leave room for in TMEM (512 columns); products into independent accumulators
@@ -430,31 +432,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint16_t* yrow = p.y + static_cast<int64_t>(live ? row : 0) * p.n;
       const uint32_t t0 = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                           static_cast<uint32_t>(half * kHalfN);
-#pragma unroll 1
+      // Drain this warp's 128 accumulator columns into registers as BF16 pairs first, release the
+      // accumulator (the next tile's products start), then store.
+      uint32_t packed[kHalfN / 2];
+#pragma unroll
       for (int c = 0; c < kHalfN; c += 32) {
         uint32_t v[32];
         tmem_load32(t0 + c, v);
         tmem_load_wait();
-        const int col0 = nt * kTileN + half * kHalfN + c;
-        if (live) {
 #pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) {
-            if (col0 + 8 * g8 >= p.n) break;
-            uint32_t w[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float lo = __fmul_rn(__fmul_rn(__uint_as_float(v[8 * g8 + 2 * j]), sx), sw);
-              const float hi =
-                  __fmul_rn(__fmul_rn(__uint_as_float(v[8 * g8 + 2 * j + 1]), sx), sw);
-              asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[j]) : "f"(hi), "f"(lo));
-            }
-            *reinterpret_cast<uint4*>(yrow + col0 + 8 * g8) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+        for (int q = 0; q < 16; ++q) {
+          const float lo = __fmul_rn(__fmul_rn(__uint_as_float(v[2 * q]), sx), sw);
+          const float hi = __fmul_rn(__fmul_rn(__uint_as_float(v[2 * q + 1]), sx), sw);
+          asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed[c / 2 + q]) : "f"(hi), "f"(lo));
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
+      const int col0 = nt * kTileN + half * kHalfN;
+      if (live) {
+#pragma unroll
+        for (int g8 = 0; g8 < kHalfN / 8; ++g8) {
+          if (col0 + 8 * g8 >= p.n) break;
+          *reinterpret_cast<uint4*>(yrow + col0 + 8 * g8) =
+              make_uint4(packed[4 * g8], packed[4 * g8 + 1], packed[4 * g8 + 2], packed[4 * g8 + 3]);
+        }
+      }
     }
   } else {
     // ---- scales into TMEM: warp w fills lanes 32*(w % 4) .. +31 of the stage's scale slot.
