@@ -526,9 +526,12 @@ def test_guided_ring_timeout_path():
     assert nv.nvfp4_get_device_status() == 0
 
 
-@pytest.mark.parametrize("cols", [16, 48, 7184])
-def test_guided_rounding_edge_values(cols):
-    x_roll = _edge_matrix(16, cols, seed=cols + 3)
+@pytest.mark.parametrize("rows,cols", [(16, 16), (16, 48), (16, 7184), (1, 1024), (77, 1024),
+                                       (5, 3072), (16, 4096)])
+def test_guided_rounding_edge_values(rows, cols):
+    """Edge values through both guided kernels: widths that are whole 1024-element units take the
+    staged one (one unit, fewer units than warps, several units per row), the others the direct one."""
+    x_roll = _edge_matrix(rows, cols, seed=cols + 3 + rows)
     (amax_h, codes_h, scales_h), (amax, codes, scales) = _oracle_record(x_roll)
     x_tr = _perturbed(x_roll, cols)
     got = nv.nvfp4_quantize_guided(x_tr, amax, codes, scales)
